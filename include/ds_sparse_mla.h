@@ -1,0 +1,210 @@
+/*
+ * ds_sparse_mla.h -- C ABI of the GB300 (sm_103a) deterministic sparse top-k
+ * and sparse MLA attention library (libds_sparse_mla.so).
+ *
+ * What the library computes
+ * -------------------------
+ * The two steps of DeepSeek-V4-style sparse MLA described on the pages
+ * "[DeepSeek-V4][Preview][DO NOT MERGE] Batch-invariant kernels for 0-diff
+ * RL" (vllm-project/vllm PR 54955), sections "Deterministic sparse top-k" and
+ * "Sparse MLA and FlashMLA", and "[Bugfix] Make DSV4 sparse MLA work
+ * end-to-end for plain decode, MTP, and DSpark" (vllm-project/vllm PR 51538),
+ * section "What is fixed":
+ *
+ *   1. ds_topk_per_row: for every row, the k positions with the largest
+ *      indexer scores under the total order (score descending, position
+ *      ascending), written in ascending position order, -1 in unused slots.
+ *   2. ds_sparse_mla_decode / ds_sparse_mla_prefill: gather the selected
+ *      entries of a paged latent KV cache (64 entries per page, 576 = 512
+ *      latent + 64 rope dims, one latent row shared by every head) and
+ *      compute out = softmax(scale * q K^T) V with V = the first 512 dims of
+ *      the same rows, plus lse = ln(sum exp(scale * q K^T)).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer (cudaMalloc'd or otherwise
+ *    device-accessible) unless stated otherwise. Nothing is allocated or
+ *    freed inside; outputs and workspaces are owned by the caller, as in the
+ *    caller-owned-output contract of "[JJ] Preallocate DeepSeek V4
+ *    padded-query output" (local-inference-lab/vllm PR 671, section
+ *    "Operation contract").
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Every call only enqueues work on it and never synchronises the
+ *    host, so calls may be captured into a CUDA graph.
+ *  - Arguments are validated on the host before anything is launched.
+ *    Unsupported shapes are a hard error (PR 54955: "missing kernel support
+ *    is a hard error rather than a silent fallback"); ds_last_error() names
+ *    the offending parameter and the allowed set (PR 51538, "SM120 gate").
+ *  - Row lengths are computed signed and clamped at 0 before any decision,
+ *    so a negative length from a padded request is an empty row, never a
+ *    huge unsigned value (PR 51538, "What is fixed").
+ *  - Offsets inside the kernels are 64-bit: tensors may exceed 2^31
+ *    elements (PR 54955, the 64-bit offset fix).
+ *  - Results never depend on the rest of the batch: every row's output is
+ *    bit-identical whether it runs alone or inside any batch, because each
+ *    row's work is split and reduced in an order fixed by k alone.
+ *  - Return value: DS_OK, or a ds_status error code. Any code other than
+ *    DS_OK or DS_ERR_CUDA means nothing was launched; DS_ERR_CUDA means a
+ *    launch failed (cudaGetLastError() reported an error).
+ */
+#ifndef DS_SPARSE_MLA_H
+#define DS_SPARSE_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DS_OK = 0,
+  DS_ERR_NULL = 1,         /* a required pointer is NULL                      */
+  DS_ERR_SHAPE = 2,        /* a size is negative or inconsistent              */
+  DS_ERR_UNSUPPORTED = 3,  /* a size is outside the supported set             */
+  DS_ERR_DTYPE = 4,        /* unknown kv_dtype                                */
+  DS_ERR_ALIGN = 5,        /* a pointer is not aligned as required            */
+  DS_ERR_WORKSPACE = 6,    /* workspace missing or smaller than required      */
+  DS_ERR_CUDA = 7          /* the CUDA runtime reported an error at launch    */
+} ds_status;
+
+typedef enum {
+  DS_KV_BF16 = 0,          /* kv row = 576 bfloat16 (1152 bytes)              */
+  DS_KV_FP8_E4M3 = 1       /* kv row = 656 bytes, layout below                */
+} ds_kv_dtype;
+
+/*
+ * FP8 KV row layout (656 bytes, 16-byte aligned): bytes [0, 512) are the
+ * 512 latent dims as OCP FP8 E4M3 codes; bytes [512, 528) are four
+ * little-endian float32 scales, one per 128-dim group (dims 0-127, 128-255,
+ * 256-383, 384-511), kept contiguous as in the FP8 KV cache of
+ * "MooreThreads/vllm-musa PR 178" (optimisation table, contiguous FP32 scale
+ * groups); bytes [528, 656) are the 64 rope dims as bfloat16. A latent value
+ * is code * scale of its group.
+ */
+#define DS_PAGE_BLOCK_SIZE 64
+#define DS_D_QK 576
+#define DS_D_V 512
+#define DS_KV_ROW_BYTES_BF16 1152
+#define DS_KV_ROW_BYTES_FP8 656
+
+/* Device-side error bits ORed into *err_flag (when err_flag != NULL). */
+#define DS_DEVERR_IDX 1      /* an idx entry other than -1 outside [0, lens[row]) */
+#define DS_DEVERR_PAGE 2     /* a block-table slot beyond bt_stride, or a page id
+                                outside [0, num_pages)                            */
+#define DS_DEVERR_ROWREQ 4   /* prefill: row_req[t] outside [0, num_requests)     */
+#define DS_DEVERR_TIMEOUT 8  /* an internal pipeline wait gave up (library bug)   */
+
+/*
+ * Message of the last error on the calling host thread ("" if none). The
+ * string is thread-local and stays valid until the next call on this thread.
+ */
+const char* ds_last_error(void);
+
+/*
+ * 1 if (num_heads, topk, page_block_size, d_qk, d_v, kv_dtype) is a shape the
+ * attention entry points accept, else 0 with ds_last_error() naming the first
+ * parameter that missed and the values that are available. Lets a caller
+ * validate a model configuration at init time instead of at its first decode
+ * (PR 51538, "SM120 gate"). Supported: num_heads in {16, 32, 64, 128}; topk a
+ * multiple of 64 in [64, 2048]; page_block_size 64; d_qk 576; d_v 512;
+ * kv_dtype DS_KV_BF16 or DS_KV_FP8_E4M3.
+ */
+int ds_supported_config(int num_heads, int topk, int page_block_size, int d_qk, int d_v,
+                        int kv_dtype);
+
+/* Workspace bytes ds_topk_per_row needs (currently 0: it needs none). */
+size_t ds_topk_workspace_size(int64_t num_rows, int64_t row_stride, int k);
+
+/*
+ * Workspace bytes ds_sparse_mla_decode / ds_sparse_mla_prefill need for
+ * num_rows query rows (decode requests or prefill tokens), num_heads heads
+ * and top-k width k: the per-split partial results (float32). The number of
+ * splits is a function of k alone. Returns 0 for an unsupported shape.
+ */
+size_t ds_sparse_mla_workspace_size(int64_t num_rows, int num_heads, int k);
+
+/*
+ * Deterministic per-row top-k ("Deterministic sparse top-k", PR 54955; length
+ * clamp and -1 padding from PR 51538, "What is fixed").
+ *
+ *  scores      float32, row-major [num_rows, row_stride]; 4-byte aligned.
+ *  row_stride  elements between consecutive rows, 1 <= row_stride <= 2^28.
+ *  num_rows    >= 0 (0 launches nothing).
+ *  row_starts  int32 [num_rows]; row_ends int32 [num_rows]. Row b ranks the
+ *              scores at positions [row_starts[b], row_starts[b] + L_b) with
+ *              L_b = clamp(row_ends[b] - row_starts[b], 0,
+ *                          row_stride - row_starts[b]),
+ *              computed signed; a row_starts[b] outside [0, row_stride] gives
+ *              L_b = 0.
+ *  k           1 <= k <= 16384.
+ *  idx_out     int32 [num_rows, k], written fully: the selected positions
+ *              RELATIVE to row_starts[b], ascending, then -1 in slots
+ *              [min(k, L_b), k). Rows with L_b <= k select every position.
+ *
+ * Order: larger score first; equal scores (-0.0 equals +0.0) by lower
+ * position; NaN ranks below -inf and NaNs tie with one another. The selected
+ * set is therefore unique and the output is bit-exact and independent of the
+ * batch. workspace may be NULL (ds_topk_workspace_size() is 0).
+ */
+int ds_topk_per_row(const float* scores, int64_t row_stride, int64_t num_rows,
+                    const int32_t* row_starts, const int32_t* row_ends, int k,
+                    int32_t* idx_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Sparse MLA decode over a paged latent KV cache ("Sparse MLA and FlashMLA",
+ * PR 54955: decode gathers the selected KV and runs sparse attention; slot
+ * arithmetic slot = block_id * block_size + offset from PR 51538).
+ *
+ *  q            bfloat16 [num_rows, num_heads, 576], 16-byte aligned.
+ *  kv_pages     DS_KV_BF16: bfloat16 [num_pages, 64, 576];
+ *               DS_KV_FP8_E4M3: uint8 [num_pages, 64, 656]. 16-byte aligned.
+ *  num_pages    >= 1.
+ *  block_table  int32 [num_rows, bt_stride]: page id of each 64-position
+ *               block of row b's context.
+ *  idx          int32 [num_rows, k]: context positions to attend to (the
+ *               output of ds_topk_per_row); -1 entries are skipped.
+ *  lens         int32 [num_rows]: context length of each row.
+ *  scale        softmax scale applied to q.K (e.g. 1/sqrt(576)).
+ *  out          bfloat16 [num_rows, num_heads, 512], 16-byte aligned.
+ *  lse          float32 [num_rows, num_heads]: natural-log sum of
+ *               exp(scale * q.K) over the valid entries (-inf if none).
+ *  workspace    >= ds_sparse_mla_workspace_size(num_rows, num_heads, k)
+ *               bytes, 256-byte aligned; contents need no initialisation.
+ *  err_flag     optional int32 device word (NULL = no report). Entries with
+ *               an idx outside [0, lens[b]) (other than -1), or whose page
+ *               lookup misses, are skipped and a DS_DEVERR_* bit is ORed in;
+ *               the kernels never trap.
+ *
+ * Entry j of row b is valid iff 0 <= idx[b,j] < lens[b], idx[b,j]/64 <
+ * bt_stride and the page id lies in [0, num_pages). A row with no valid entry
+ * gives out = 0 and lse = -inf.
+ */
+int ds_sparse_mla_decode(const void* q, const void* kv_pages, int kv_dtype, int64_t num_pages,
+                         const int32_t* block_table, int64_t bt_stride,
+                         const int32_t* idx, const int32_t* lens,
+                         int64_t num_rows, int num_heads, int k, float scale,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         int32_t* err_flag, void* stream);
+
+/*
+ * Sparse MLA prefill: as decode, with one query row per token. Token t reads
+ * block-table row row_req[t] (int32 [num_tokens], in [0, num_requests)) and
+ * is computed on its own, never through a batch-level plan ("Batch-invariant
+ * prefill chunks each request independently", PR 54955). block_table is
+ * int32 [num_requests, bt_stride]; idx, lens, q, out and lse are indexed by
+ * token. A row_req outside [0, num_requests) gives out = 0, lse = -inf and
+ * sets DS_DEVERR_ROWREQ.
+ */
+int ds_sparse_mla_prefill(const void* q, const void* kv_pages, int kv_dtype, int64_t num_pages,
+                          const int32_t* block_table, int64_t bt_stride, int64_t num_requests,
+                          const int32_t* row_req, const int32_t* idx, const int32_t* lens,
+                          int64_t num_tokens, int num_heads, int k, float scale,
+                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                          int32_t* err_flag, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS_SPARSE_MLA_H */

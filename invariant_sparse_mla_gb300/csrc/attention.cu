@@ -1,0 +1,644 @@
+// Sparse MLA attention over a paged latent KV cache, for decode and prefill.
+//
+// Computes, per query row and head, out = softmax(scale * q K^T) V over the
+// row's selected entries, V being the first 512 of the 576 latent dims of the
+// same rows ("[DeepSeek-V4][Preview][DO NOT MERGE] Batch-invariant kernels for
+// 0-diff RL", section "Sparse MLA and FlashMLA": decode gathers the selected
+// KV and runs sparse attention; prefill handles each token on its own). The
+// page lookup of a context position is page = block_table[row][pos / 64],
+// slot = pos % 64 ("[Bugfix] Make DSV4 sparse MLA work end-to-end ...",
+// section "What is fixed").
+//
+// Work decomposition (fixed by k alone, never by the batch): a CTA owns one
+// (query row, split of 512 entries, group of <= 64 heads). A fixed-order
+// combine kernel merges the splits. Within a CTA:
+//
+//   producer warps 4-7  gather 64-entry tiles of 1152-byte bf16 rows into a
+//                       128-byte-swizzled shared-memory tile (FP8 rows are
+//                       dequantised to bf16 on the way), double buffered;
+//   MMA warp 8          one thread issues tcgen05 MMAs:
+//                         S   = Q K^T      M=128 (heads), N=64, K=576 -> TMEM
+//                         O^T += V^T P^T   M=128 (dv block), N=heads, K=64
+//                       The same swizzled tile is the K-major B operand of
+//                       the first and the MN-major A operand of the second.
+//   softmax warps 0-3   read S from TMEM (one head per TMEM lane), keep a
+//                       running max m and sum l per head, write P (bf16) to
+//                       shared memory, and rescale O^T in TMEM only when a
+//                       head's max grows by more than 2^8 (exact: p <= 256
+//                       is kept relative to the stored max).
+//
+// Rows of the QK MMA beyond the head group are never read: the A descriptor
+// simply continues into the next swizzle atoms, and a D row depends only on
+// its own A row. Every wait is bounded; a timeout sets DS_DEVERR_TIMEOUT and
+// the CTA winds down, frees its TMEM and exits.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsmla {
+
+namespace {
+
+constexpr int kD = 576;
+constexpr int kDv = 512;
+constexpr int kRowBytesBf16 = kD * 2;                 // 1152
+constexpr int kRowBytesFp8 = 656;
+constexpr int kChunks = kRowBytesBf16 / 16;           // 72 16-byte chunks per bf16 row
+constexpr int kTile = kTileEntries;                   // 64
+constexpr int kStageBytes = kTile * kRowBytesBf16;    // 73728
+constexpr int kAtomStride = kTile * 128;              // bytes between 64-dim column blocks
+constexpr int kThreads = 288;                         // 9 warps
+constexpr int kSCols = 64;                            // TMEM columns of one S buffer
+constexpr int kOCol = 2 * kSCols;                     // first TMEM column of O^T
+constexpr float kRescaleThreshold = 8.0f;             // log2 units
+
+// Error bits (match DS_DEVERR_* in the public header).
+constexpr int kErrIdx = 1, kErrPage = 2, kErrRowReq = 4, kErrTimeout = 8;
+
+template <int HG>
+struct Layout {
+  static constexpr int kQBytes = HG * kRowBytesBf16;
+  static constexpr int kQ = 0;
+  static constexpr int kKV0 = kQ + kQBytes;
+  static constexpr int kKV1 = kKV0 + kStageBytes;
+  static constexpr int kP = kKV1 + kStageBytes;
+  static constexpr int kPBytes = HG * 128;
+  static constexpr int kMisc = kP + kPBytes;
+  // misc: barriers, valid masks, alphas, tmem address
+  static constexpr int kBars = kMisc;                         // 16 x u64 reserved
+  static constexpr int kMask = kBars + 16 * 8;                 // kSplitTiles x u64
+  static constexpr int kAlpha = kMask + kSplitTiles * 8;       // 2 x 64 floats
+  static constexpr int kTmemSlot = kAlpha + 2 * 64 * 4;        // u32
+  static constexpr int kNeff = kTmemSlot + 4;                  // int
+  static constexpr int kEnd = kNeff + 12;
+  static constexpr int kSmemBytes = kEnd + 1024;               // + alignment slack
+  static constexpr uint32_t kTmemCols = (kOCol + 4 * HG) <= 256 ? 256u : 512u;
+};
+
+// Barrier slots in the misc area.
+enum Bar { kQFull = 0, kKvFull0 = 1, kKvFull1 = 2, kKvEmpty0 = 3, kKvEmpty1 = 4,
+           kSFull0 = 5, kSFull1 = 6, kPFull = 7, kPvDone = 8, kMmaDone = 9, kNumBars = 10 };
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Byte offset of 16-byte chunk `c` (of 72) of tile row `r` in a 128-byte
+// swizzled K-major tile whose 64-dim column blocks are `atom_stride` apart.
+__device__ __forceinline__ uint32_t swz_off(int r, int c, int atom_stride) {
+  return (uint32_t)((c >> 3) * atom_stride + (r >> 3) * 1024 + (r & 7) * 128 +
+                    (((c & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 8 E4M3 codes (little-endian in `lo`, `hi`) times `scale` -> 8 bf16 (uint4).
+__device__ __forceinline__ uint4 dequant8(uint32_t lo, uint32_t hi, float scale) {
+  float f[8];
+  const uint32_t w[2] = {lo, hi};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[i] >> (16 * j)) & 0xFFFFu);
+      const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+      const __half2 hh = *reinterpret_cast<const __half2*>(&h);
+      const float2 ff = __half22float2(hh);
+      f[i * 4 + j * 2 + 0] = ff.x * scale;
+      f[i * 4 + j * 2 + 1] = ff.y * scale;
+    }
+  }
+  uint4 r;
+  r.x = pack_bf16x2(f[0], f[1]);
+  r.y = pack_bf16x2(f[2], f[3]);
+  r.z = pack_bf16x2(f[4], f[5]);
+  r.w = pack_bf16x2(f[6], f[7]);
+  return r;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+struct KParams {
+  const __nv_bfloat16* q;
+  const uint8_t* kv;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int64_t num_bt_rows;
+  const int32_t* row_req;
+  const int32_t* idx;
+  const int32_t* lens;
+  int64_t R;
+  int H;
+  int k;
+  int num_splits;
+  int num_hg;
+  float scale_log2;
+  float* part_o;
+  float* part_m;
+  float* part_l;
+  int32_t* err;
+};
+
+template <int HG, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KParams p) {
+  using LY = Layout<HG>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kBars);
+  uint64_t* vmask = reinterpret_cast<uint64_t*>(smem + LY::kMask);
+  float* alpha_s = reinterpret_cast<float*>(smem + LY::kAlpha);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kTmemSlot);
+  int* neff_s = reinterpret_cast<int*>(smem + LY::kNeff);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  int64_t bid = blockIdx.x;
+  const int hg = (int)(bid % p.num_hg);
+  bid /= p.num_hg;
+  const int split = (int)(bid % p.num_splits);
+  const int64_t row = bid / p.num_splits;
+
+  int64_t bt_row = row;
+  bool row_ok = true;
+  if (p.row_req != nullptr) {
+    bt_row = p.row_req[row];
+    row_ok = bt_row >= 0 && bt_row < p.num_bt_rows;
+  }
+  int64_t len = p.lens[row];
+  if (len < 0) len = 0;
+
+  const int j0 = split * kSplitEntries;
+  const int j1 = min(p.k, j0 + kSplitEntries);
+  const int32_t* idx_row = p.idx + row * (int64_t)p.k;
+
+  // Number of tiles up to the last entry that is not -1 padding.
+  if (tid == 0) *neff_s = 0;
+  __syncthreads();
+  {
+    int last = -1;
+    for (int j = j0 + tid; j < j1; j += kThreads)
+      if (idx_row[j] != -1) last = j;
+    if (last >= 0) atomicMax(neff_s, (last - j0) / kTile + 1);
+  }
+  __syncthreads();
+  const int n_eff = row_ok ? *neff_s : 0;
+  const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
+
+  if (!row_ok && tid == 0 && p.err != nullptr) atomicOr(p.err, kErrRowReq);
+  if (n_eff == 0) {  // nothing to attend to in this split
+    if (tid < HG) {
+      p.part_m[part_base + tid] = -INFINITY;
+      p.part_l[part_base + tid] = 0.0f;
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    // 128-count barriers take one arrival per producer (or softmax) thread;
+    // the others one tcgen05.commit.
+    for (int i = 0; i < kNumBars; ++i) {
+      const bool per_thread = i == kQFull || i == kKvFull0 || i == kKvFull1 || i == kPFull;
+      mbar_init(&bars[i], per_thread ? 128u : 1u);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, LY::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  uint64_t* pv_done = &bars[kPvDone];
+  uint64_t* mma_done = &bars[kMmaDone];
+
+  bool failed = false;
+
+  if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ producers
+    const int ptid = tid - 128;
+    const int pw = warp - 4;
+    // Q rows of this head group.
+    const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
+    for (int c = ptid; c < HG * kChunks; c += 128) {
+      const int h = c / kChunks, ch = c - h * kChunks;
+      cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    mbar_arrive(&bars[kQFull]);
+
+    int err_bits = 0;
+    for (int t = 0; t < n_eff && !failed; ++t) {
+      const int stage = t & 1;
+      // The warp decides together, so its shuffles below never diverge.
+      const bool ok = t < 2 || mbar_wait(&bars[kKvEmpty0 + stage], ((t >> 1) - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      // Row lookup: lane r (< 16) resolves tile row 16*pw + r.
+      const int r = lane & 15;
+      const int j = j0 + t * kTile + pw * 16 + r;
+      const int pos = idx_row[j];
+      bool valid = pos >= 0 && (int64_t)pos < len;
+      int64_t grow = -1;
+      if (valid) {
+        const int64_t blk = pos >> 6;
+        if (blk < p.bt_stride) {
+          const int64_t page = p.block_table[bt_row * p.bt_stride + blk];
+          if (page >= 0 && page < p.num_pages) {
+            grow = page * 64 + (pos & 63);
+          } else {
+            valid = false;
+            err_bits |= kErrPage;
+          }
+        } else {
+          valid = false;
+          err_bits |= kErrPage;
+        }
+      } else if (pos != -1) {
+        err_bits |= kErrIdx;
+      }
+      const uint32_t ballot = __ballot_sync(0xffffffffu, valid) & 0xFFFFu;
+      if (lane == 0)
+        reinterpret_cast<uint16_t*>(&vmask[t])[pw] = (uint16_t)ballot;
+
+      const uint32_t stage_base = sbase + (stage ? LY::kKV1 : LY::kKV0);
+      if constexpr (!FP8) {
+        for (int rr = 0; rr < 16; ++rr) {
+          const int64_t g = __shfl_sync(0xffffffffu, grow, rr);
+          const int tr = pw * 16 + rr;
+          const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
+          const uint32_t nbytes = g >= 0 ? 16u : 0u;
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            const int c = lane + 32 * i;
+            if (c < kChunks) cp_async_16(stage_base + swz_off(tr, c, kAtomStride), src + c * 16, nbytes);
+          }
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+      } else {
+        for (int r0 = 0; r0 < 16; r0 += 4) {
+          uint2 codes[4][2];
+          float scl[4][2];
+          uint4 rope[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int64_t g = __shfl_sync(0xffffffffu, grow, r0 + u);
+            const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesFp8;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int c = lane + 32 * i;  // latent output chunk 0..63
+              if (g >= 0) {
+                codes[u][i] = *reinterpret_cast<const uint2*>(src + c * 8);
+                scl[u][i] = *reinterpret_cast<const float*>(src + 512 + (c >> 4) * 4);
+              } else {
+                codes[u][i] = make_uint2(0u, 0u);
+                scl[u][i] = 0.0f;
+              }
+            }
+            rope[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (lane < 8 && g >= 0) rope[u] = *reinterpret_cast<const uint4*>(src + 528 + lane * 16);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int tr = pw * 16 + r0 + u;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int c = lane + 32 * i;
+              st_shared_v4(stage_base + swz_off(tr, c, kAtomStride),
+                           dequant8(codes[u][i].x, codes[u][i].y, scl[u][i]));
+            }
+            if (lane < 8) st_shared_v4(stage_base + swz_off(tr, 64 + lane, kAtomStride), rope[u]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[kKvFull0 + stage]);
+    }
+    cp_async_wait_all();
+    if (err_bits && p.err != nullptr) atomicOr(p.err, err_bits);
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, HG, 1, 0);
+      const uint32_t q_addr = sbase + LY::kQ;
+      const uint32_t p_addr = sbase + LY::kP;
+      auto issue_pv = [&](int t) {
+        const uint32_t kv_addr = sbase + ((t & 1) ? LY::kKV1 : LY::kKV0);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = make_sw128_desc(kv_addr + 2 * b * kAtomStride + kk * 2048,
+                                               kAtomStride, 1024);
+            const uint64_t bd = make_sw128_desc(p_addr + kk * 32, 16, 1024);
+            mma_bf16_ss(tmem + kOCol + b * HG, a, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+      };
+      if (!mbar_wait(&bars[kQFull], 0)) failed = true;
+      for (int t = 0; t < n_eff && !failed; ++t) {
+        const int stage = t & 1;
+        if (!mbar_wait(&bars[kKvFull0 + stage], (t >> 1) & 1)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kv_addr = sbase + (stage ? LY::kKV1 : LY::kKV0);
+#pragma unroll 4
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const int ka = kk >> 2;
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t a = make_sw128_desc(q_addr + ka * (HG * 128) + off, 16, 1024);
+          const uint64_t b = make_sw128_desc(kv_addr + ka * kAtomStride + off, 16, 1024);
+          mma_bf16_ss(tmem + stage * kSCols, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[kSFull0 + stage]);
+        if (t >= 1) {
+          if (!mbar_wait(&bars[kPFull], (t - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t - 1);
+          mma_commit(&bars[kKvEmpty0 + ((t - 1) & 1)]);
+          mma_commit(pv_done);
+        }
+      }
+      if (!failed) {
+        if (mbar_wait(&bars[kPFull], (n_eff - 1) & 1)) {
+          tc_fence_after();
+          issue_pv(n_eff - 1);
+          mma_commit(pv_done);
+        } else {
+          failed = true;
+        }
+      }
+      // Drain: wait until every MMA issued above has completed.
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int h = tid;               // TMEM lane == S row == head in group
+    const bool warp_has_heads = warp * 32 < HG;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint8_t* prow = smem + LY::kP + (h >> 3) * 1024 + (h & 7) * 128;
+    float m = -INFINITY, l = 0.0f;
+    float s[kSCols];
+    // All four softmax warps meet at named barriers (ids 1-3), so every
+    // timeout decision is made jointly: either all leave the loop or none.
+    for (int t = 0; t < n_eff; ++t) {
+      const int sb = t & 1;
+      const bool ok = mbar_wait(&bars[kSFull0 + sb], (t >> 1) & 1);
+      bool need = false;
+      if (ok) {
+        tc_fence_after();
+        if (warp_has_heads) {
+          tmem_ld32_sync(tmem + lane_base + sb * kSCols, s);
+          tmem_ld32_sync(tmem + lane_base + sb * kSCols + 32, s + 32);
+          const uint64_t mask = vmask[t];
+          float mt = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < kSCols; ++j) {
+            s[j] = ((mask >> j) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
+            mt = fmaxf(mt, s[j]);
+          }
+          float a = 1.0f;
+          if (mt > m + kRescaleThreshold) {
+            a = (m == -INFINITY) ? 0.0f : ex2(m - mt);
+            need = t > 0;
+            l *= a;
+            m = mt;
+          }
+          if (h < HG) alpha_s[sb * 64 + h] = a;
+        }
+      }
+      if (named_bar_or(1, 128, !ok)) {
+        failed = true;
+        break;
+      }
+      const bool any = named_bar_or(2, 128, need);
+      const bool ok2 = t == 0 || mbar_wait(pv_done, (t - 1) & 1);
+      if (named_bar_or(3, 128, !ok2)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      if (any) {
+        // O^T lanes are dv rows; columns are heads. Scale column h by alpha[h].
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+#pragma unroll
+          for (int c = 0; c < HG / 16; ++c) {
+            float v[16];
+            const uint32_t addr = tmem + lane_base + kOCol + b * HG + 16 * c;
+            tmem_ld16_sync(addr, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= alpha_s[sb * 64 + 16 * c + i];
+            tmem_st16(addr, v);
+          }
+        }
+        tmem_wait_st();
+      }
+      if (warp_has_heads && h < HG) {
+        float lsum = 0.0f;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float p0 = (m == -INFINITY) ? 0.0f : ex2(s[8 * c8 + 2 * i] - m);
+            const float p1 = (m == -INFINITY) ? 0.0f : ex2(s[8 * c8 + 2 * i + 1] - m);
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            const float2 pr = __bfloat1622float2(pb);
+            lsum += pr.x;
+            lsum += pr.y;
+            w[i] = *reinterpret_cast<const uint32_t*>(&pb);
+          }
+          const uint32_t dst = smem_u32(prow) + ((c8 ^ (h & 7)) << 4);
+          st_shared_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+        }
+        l += lsum;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[kPFull]);
+    }
+    if (!failed && !mbar_wait(pv_done, (n_eff - 1) & 1)) failed = true;
+    if (!failed) {
+      tc_fence_after();
+      // Epilogue: partial O (unnormalised, relative to m), m and l.
+      const int dv_lane = warp * 32 + lane;
+      float* po = p.part_o + part_base * kDv;
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+#pragma unroll
+        for (int c = 0; c < HG / 16; ++c) {
+          float v[16];
+          tmem_ld16_sync(tmem + lane_base + kOCol + b * HG + 16 * c, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) po[(int64_t)(16 * c + i) * kDv + 128 * b + dv_lane] = v[i];
+        }
+      }
+      if (h < HG) {
+        p.part_m[part_base + h] = m;
+        p.part_l[part_base + h] = l;
+      }
+    }
+  }
+
+  if (failed && p.err != nullptr) atomicOr(p.err, kErrTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 8) tmem_dealloc(tmem, LY::kTmemCols);
+}
+
+// Merges the splits of one (row, head) in split order: M = max m_s,
+// out = sum 2^(m_s - M) O_s / sum 2^(m_s - M) l_s, lse = (M + log2 L) ln 2.
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_m,
+                                                      const float* __restrict__ part_l,
+                                                      int64_t R, int H, int S,
+                                                      __nv_bfloat16* __restrict__ out,
+                                                      float* __restrict__ lse) {
+  const int64_t rh = blockIdx.x;  // row * H + h
+  const int t = threadIdx.x;
+  const int64_t RH = R * H;
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[s * RH + rh]);
+  __nv_bfloat16* o = out + rh * kDv + 4 * t;
+  if (M == -INFINITY) {
+    *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
+    if (t == 0) lse[rh] = -INFINITY;
+    return;
+  }
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float L = 0.0f;
+  for (int s = 0; s < S; ++s) {
+    const float ms = part_m[s * RH + rh];
+    if (ms == -INFINITY) continue;
+    const float w = ex2(ms - M);
+    L += w * part_l[s * RH + rh];
+    const float4 v = *reinterpret_cast<const float4*>(part_o + (s * RH + rh) * kDv + 4 * t);
+    acc[0] += w * v.x;
+    acc[1] += w * v.y;
+    acc[2] += w * v.z;
+    acc[3] += w * v.w;
+  }
+  const float inv = 1.0f / L;
+  uint2 r;
+  r.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  r.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  *reinterpret_cast<uint2*>(o) = r;
+  if (t == 0) lse[rh] = (M + log2f(L)) * 0.69314718055994530942f;
+}
+
+template <int HG, bool FP8>
+cudaError_t launch_split(const KParams& kp, int64_t blocks, cudaStream_t stream) {
+  using LY = Layout<HG>;
+  static std::atomic<bool> attr_set{false};
+  auto kern = sparse_mla_split_kernel<HG, FP8>;
+  if (!attr_set.load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         LY::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set.store(true, std::memory_order_release);
+  }
+  kern<<<(unsigned)blocks, kThreads, LY::kSmemBytes, stream>>>(kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(int64_t R, int H, int k) {
+  const int64_t S = num_splits_for_k(k);
+  const int64_t n = S * R * H;
+  const size_t o = (size_t)n * kDv * sizeof(float);
+  const size_t ml = ((size_t)n * sizeof(float) + 255) & ~size_t(255);
+  return o + 2 * ml;
+}
+
+AttnWorkspace attn_workspace_carve(void* base, int64_t R, int H, int k) {
+  const int64_t S = num_splits_for_k(k);
+  const int64_t n = S * R * H;
+  const size_t o = (size_t)n * kDv * sizeof(float);
+  const size_t ml = ((size_t)n * sizeof(float) + 255) & ~size_t(255);
+  AttnWorkspace w;
+  w.part_o = reinterpret_cast<float*>(base);
+  w.part_m = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(base) + o);
+  w.part_l = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(base) + o + ml);
+  return w;
+}
+
+cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream) {
+  if (a.R == 0) return cudaSuccess;
+  const int HG = a.H < 64 ? a.H : 64;
+  KParams kp;
+  kp.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  kp.kv = reinterpret_cast<const uint8_t*>(a.kv);
+  kp.num_pages = a.num_pages;
+  kp.block_table = a.block_table;
+  kp.bt_stride = a.bt_stride;
+  kp.num_bt_rows = a.num_bt_rows;
+  kp.row_req = a.row_req;
+  kp.idx = a.idx;
+  kp.lens = a.lens;
+  kp.R = a.R;
+  kp.H = a.H;
+  kp.k = a.k;
+  kp.num_splits = num_splits_for_k(a.k);
+  kp.num_hg = a.H / HG;
+  kp.scale_log2 = a.scale * 1.4426950408889634f;
+  AttnWorkspace ws = attn_workspace_carve(a.workspace, a.R, a.H, a.k);
+  kp.part_o = ws.part_o;
+  kp.part_m = ws.part_m;
+  kp.part_l = ws.part_l;
+  kp.err = a.err_flag;
+  const int64_t blocks = a.R * kp.num_splits * kp.num_hg;
+  const bool fp8 = a.kv_dtype == 1;
+  cudaError_t e;
+  if (HG == 64)
+    e = fp8 ? launch_split<64, true>(kp, blocks, stream) : launch_split<64, false>(kp, blocks, stream);
+  else if (HG == 32)
+    e = fp8 ? launch_split<32, true>(kp, blocks, stream) : launch_split<32, false>(kp, blocks, stream);
+  else
+    e = fp8 ? launch_split<16, true>(kp, blocks, stream) : launch_split<16, false>(kp, blocks, stream);
+  if (e != cudaSuccess) return e;
+  combine_kernel<<<(unsigned)(a.R * a.H), 128, 0, stream>>>(
+      ws.part_o, ws.part_m, ws.part_l, a.R, a.H, kp.num_splits,
+      reinterpret_cast<__nv_bfloat16*>(a.out), a.lse);
+  return cudaGetLastError();
+}
+
+}  // namespace dsmla

@@ -1,0 +1,54 @@
+// Declarations shared by the host API (api.cu) and the kernel files.
+#pragma once
+
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+namespace dsmla {
+
+// Entries per attention tile and tiles per split. The split count of a call
+// is ceil(k / kSplitEntries): a function of k alone, so a row's reduction
+// order never depends on the batch.
+constexpr int kTileEntries = 64;
+constexpr int kSplitTiles = 8;
+constexpr int kSplitEntries = kTileEntries * kSplitTiles;
+
+inline int num_splits_for_k(int k) { return (k + kSplitEntries - 1) / kSplitEntries; }
+
+struct AttnArgs {
+  const void* q;             // bf16 [R, H, 576]
+  const void* kv;            // pool base
+  int kv_dtype;              // 0 bf16, 1 fp8
+  int64_t num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int64_t num_bt_rows;       // rows of block_table
+  const int32_t* row_req;    // nullptr: row r reads block-table row r
+  const int32_t* idx;        // [R, k]
+  const int32_t* lens;       // [R]
+  int64_t R;
+  int H;
+  int k;
+  float scale;
+  void* out;                 // bf16 [R, H, 512]
+  float* lse;                // [R, H]
+  void* workspace;
+  int32_t* err_flag;         // may be nullptr
+};
+
+// Workspace layout of the attention path: partial O, m and l per split.
+struct AttnWorkspace {
+  float* part_o;  // [S, R, H, 512]
+  float* part_m;  // [S, R, H]  (log2 domain, scale folded in)
+  float* part_l;  // [S, R, H]
+};
+
+size_t attn_workspace_bytes(int64_t R, int H, int k);
+AttnWorkspace attn_workspace_carve(void* base, int64_t R, int H, int k);
+
+cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const int32_t* starts,
+                        const int32_t* ends, int k, int32_t* out, cudaStream_t stream);
+
+cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace dsmla

@@ -1,0 +1,81 @@
+"""Test plumbing shared by the GPU parity tests (no method arithmetic here).
+
+Moves tensors between the device and the oracle's NumPy views, cuts a
+compact page pool for sampled rows of workloads whose full pool is too large
+to copy to the host, and holds the tolerance check.
+"""
+
+import numpy as np
+import torch
+
+# Per element |gpu - ref| <= ATOL + RTOL * |ref| on out; lse within LSE_ATOL.
+ATOL = {"bf16": 2e-2, "fp8": 4e-2}
+RTOL = 1e-2
+LSE_ATOL = 1e-2
+
+
+def ensure_built():
+    import invariant_sparse_mla_gb300 as ds
+    from invariant_sparse_mla_gb300 import build as b
+    import os
+    if not os.path.exists(b.lib_path()):
+        b.build()
+    return ds
+
+
+def q_bits(q):
+    return q.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def kv_np(kv, kv_dtype):
+    kv = kv.cpu()
+    if kv_dtype == "bf16":
+        return kv.view(torch.int16).numpy().view(np.uint16)
+    return kv.numpy()
+
+
+def compact_rows(case, rows, idx):
+    """Oracle inputs for a sample of rows, with a pool of only the pages used.
+
+    Returns (q_bits, kv, block_table, idx, lens) for the sampled rows; the
+    block table is remapped into a pool holding just the pages the sampled
+    idx entries touch (every other slot points at page 0 and is never read
+    by a valid entry).
+    """
+    rows = list(rows)
+    bt_full = case.block_table.cpu().numpy()
+    req = case.row_req.cpu().numpy()[rows]
+    idx_s = idx[rows]
+    lens = case.lens.cpu().numpy()[rows]
+    blocks = []
+    for i in range(len(rows)):
+        pos = idx_s[i][idx_s[i] >= 0]
+        blocks.append(np.unique(pos // 64))
+    pages = sorted({int(bt_full[req[i], b]) for i in range(len(rows)) for b in blocks[i]
+                    if 0 <= b < bt_full.shape[1]})
+    remap = {p: n for n, p in enumerate(pages)}
+    bt = np.zeros((len(rows), bt_full.shape[1]), dtype=np.int64)
+    for i in range(len(rows)):
+        for b in blocks[i]:
+            if 0 <= b < bt_full.shape[1]:
+                bt[i, b] = remap[int(bt_full[req[i], b])]
+    page_idx = torch.tensor(pages if pages else [0], dtype=torch.long, device=case.kv_pages.device)
+    kv = kv_np(case.kv_pages.index_select(0, page_idx), case.kv_dtype)
+    return q_bits(case.q[rows]), kv, bt, idx_s, lens
+
+
+def assert_close(out, lse, ref_out, ref_lse, kv_dtype, what=""):
+    o = out.float().cpu().numpy() if isinstance(out, torch.Tensor) else out
+    l = lse.cpu().numpy() if isinstance(lse, torch.Tensor) else lse
+    tol = ATOL[kv_dtype] + RTOL * np.abs(ref_out)
+    err = np.abs(o - ref_out)
+    bad = ~(err <= tol)
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} out elements off; max abs err "
+                           f"{np.nanmax(err):.4g} at {np.unravel_index(np.nanargmax(err), err.shape)}")
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(l), fin), f"{what}: lse finiteness differs"
+    assert np.all(np.isneginf(l[~fin])), f"{what}: empty rows must give lse = -inf"
+    if fin.any():
+        lerr = np.abs(l[fin] - ref_lse[fin])
+        assert lerr.max() <= LSE_ATOL, f"{what}: lse max err {lerr.max():.4g}"
+    return float(np.nanmax(err)) if err.size else 0.0

@@ -1,0 +1,165 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before launching anything.
+
+Host validation follows the pages' contract: unsupported shapes are a hard
+error ("Batch-invariant kernels for 0-diff RL", PR 54955), checked before the
+kernel launch ("Preallocate DeepSeek V4 padded-query output", PR 671,
+"Operation contract"), with a message naming the parameter that missed and
+what is available ("Make DSV4 sparse MLA work end-to-end", PR 51538,
+"SM120 gate"). None of these calls reaches the CUDA runtime.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from harness import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ds_sparse_mla.h")
+
+DS_OK, DS_ERR_NULL, DS_ERR_SHAPE, DS_ERR_UNSUPPORTED, DS_ERR_DTYPE, DS_ERR_ALIGN, \
+    DS_ERR_WORKSPACE, DS_ERR_CUDA = range(8)
+
+# Fake, never-dereferenced device addresses: validation must fail before use.
+A = 0x7F0000000000
+
+
+@pytest.fixture(scope="module")
+def ds():
+    return ensure_built()
+
+
+@pytest.fixture(scope="module")
+def L(ds):
+    return ds.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("ds_topk_per_row", "ds_sparse_mla_decode", "ds_sparse_mla_prefill",
+                 "ds_last_error", "ds_supported_config"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(ds, L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(ds.EXPORTED) <= set(declared_functions())
+
+
+def _err(L):
+    return L.ds_last_error().decode()
+
+
+def test_supported_config_matrix(L):
+    for h in (16, 32, 64, 128):
+        for k in (64, 128, 512, 2048):
+            for kvd in (0, 1):
+                assert L.ds_supported_config(h, k, 64, 576, 512, kvd) == 1
+    cases = [((48, 2048, 64, 576, 512, 0), "num_heads"),
+             ((64, 100, 64, 576, 512, 0), "topk"),
+             ((64, 4096, 64, 576, 512, 0), "topk"),
+             ((64, 0, 64, 576, 512, 0), "topk"),
+             ((64, 2048, 128, 576, 512, 0), "page_block_size"),
+             ((64, 2048, 64, 512, 512, 0), "d_qk"),
+             ((64, 2048, 64, 576, 576, 0), "d_v"),
+             ((64, 2048, 64, 576, 512, 7), "kv_dtype")]
+    for args, name in cases:
+        assert L.ds_supported_config(*args) == 0
+        msg = _err(L)
+        assert name in msg and "available" in msg, msg
+
+
+def test_workspace_sizes(L):
+    # splits = ceil(k / 512); per split: R*H*(512 + 2) floats, m/l 256-aligned.
+    def want(R, H, k):
+        n = -(-k // 512) * R * H
+        ml = (n * 4 + 255) // 256 * 256
+        return n * 512 * 4 + 2 * ml
+    for R, H, k in [(1, 16, 64), (32, 64, 2048), (128, 128, 2048), (4096, 128, 2048), (3, 32, 576)]:
+        if k % 64:
+            assert L.ds_sparse_mla_workspace_size(R, H, k) == 0
+        else:
+            assert L.ds_sparse_mla_workspace_size(R, H, k) == want(R, H, k)
+    assert L.ds_sparse_mla_workspace_size(4, 48, 2048) == 0
+    assert L.ds_topk_workspace_size(100, 1000, 10) == 0
+
+
+def _topk(L, scores=A, stride=1024, rows=4, starts=A, ends=A, k=16, out=A):
+    return L.ds_topk_per_row(scores, stride, rows, starts, ends, k, out, None, 0, None)
+
+
+def test_topk_rejects_bad_arguments(L):
+    assert _topk(L, k=0) == DS_ERR_UNSUPPORTED and "k=0" in _err(L)
+    assert _topk(L, k=20000) == DS_ERR_UNSUPPORTED
+    assert _topk(L, stride=0) == DS_ERR_UNSUPPORTED and "row_stride" in _err(L)
+    assert _topk(L, rows=-1) == DS_ERR_SHAPE
+    assert _topk(L, scores=None) == DS_ERR_NULL and "scores" in _err(L)
+    assert _topk(L, starts=None) == DS_ERR_NULL and "row_starts" in _err(L)
+    assert _topk(L, out=None) == DS_ERR_NULL and "idx_out" in _err(L)
+    assert _topk(L, scores=A + 2) == DS_ERR_ALIGN
+    # Zero rows is a valid empty call: nothing is launched.
+    assert _topk(L, rows=0, scores=None, starts=None, ends=None, out=None) == DS_OK
+
+
+def _decode(L, **kw):
+    a = dict(q=A, kv=A, kvd=0, pages=16, bt=A, bts=8, idx=A, lens=A, R=4, H=64, k=2048,
+             scale=0.04, out=A, lse=A, ws=A, wsb=1 << 40, err=None)
+    a.update(kw)
+    return L.ds_sparse_mla_decode(a["q"], a["kv"], a["kvd"], a["pages"], a["bt"], a["bts"],
+                                  a["idx"], a["lens"], a["R"], a["H"], a["k"], a["scale"], a["out"],
+                                  a["lse"], a["ws"], a["wsb"], a["err"], None)
+
+
+def test_decode_rejects_bad_arguments(L):
+    assert _decode(L, H=48) == DS_ERR_UNSUPPORTED and "num_heads=48" in _err(L)
+    assert _decode(L, k=100) == DS_ERR_UNSUPPORTED and "topk=100" in _err(L)
+    assert _decode(L, kvd=5) == DS_ERR_DTYPE and "kv_dtype" in _err(L)
+    assert _decode(L, R=-2) == DS_ERR_SHAPE
+    assert _decode(L, pages=0) == DS_ERR_SHAPE and "num_pages" in _err(L)
+    assert _decode(L, bts=0) == DS_ERR_SHAPE and "bt_stride" in _err(L)
+    assert _decode(L, scale=float("nan")) == DS_ERR_SHAPE and "scale" in _err(L)
+    for name in ("q", "kv", "bt", "idx", "lens", "out", "lse", "ws"):
+        assert _decode(L, **{name: None}) == DS_ERR_NULL, name
+    assert _decode(L, q=A + 8) == DS_ERR_ALIGN and "q must be 16-byte" in _err(L)
+    assert _decode(L, kv=A + 4) == DS_ERR_ALIGN and "kv_pages" in _err(L)
+    assert _decode(L, ws=A + 16) == DS_ERR_ALIGN and "workspace" in _err(L)
+    assert _decode(L, err=A + 2) == DS_ERR_ALIGN and "err_flag" in _err(L)
+    need = L.ds_sparse_mla_workspace_size(4, 64, 2048)
+    assert _decode(L, wsb=need - 1) == DS_ERR_WORKSPACE and str(need) in _err(L)
+    assert _decode(L, R=0, q=None, kv=None, out=None) in (DS_OK, DS_ERR_NULL)
+
+
+def test_prefill_requires_row_req(L):
+    r = L.ds_sparse_mla_prefill(A, A, 0, 16, A, 8, 1, None, A, A, 4, 64, 2048, 0.04, A, A, A,
+                                1 << 40, None, None)
+    assert r == DS_ERR_NULL and "row_req" in _err(L)
+    r = L.ds_sparse_mla_prefill(A, A, 0, 16, A, 8, 0, A, A, A, 4, 64, 2048, 0.04, A, A, A,
+                                1 << 40, None, None)
+    assert r == DS_ERR_SHAPE and "num_requests" in _err(L)
+
+
+def test_last_error_clears_on_success(L):
+    assert L.ds_supported_config(7, 64, 64, 576, 512, 0) == 0
+    assert _err(L) != ""
+    assert L.ds_supported_config(64, 64, 64, 576, 512, 0) == 1
+    assert _err(L) == ""
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors(ds):
+    import torch
+    with pytest.raises(ValueError):
+        ds.topk_per_row(torch.zeros(2, 8), torch.zeros(2, dtype=torch.int32),
+                        torch.zeros(2, dtype=torch.int32), 4)
+    with pytest.raises(TypeError):
+        ds.topk_per_row(torch.zeros(2, 8, dtype=torch.float64), torch.zeros(2, dtype=torch.int32),
+                        torch.zeros(2, dtype=torch.int32), 4)

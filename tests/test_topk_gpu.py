@@ -1,0 +1,170 @@
+"""GPU parity of ds_topk_per_row against the oracle: bit-exact indices.
+
+Covers the named workloads (tiny decode with ties, the TP2-shaped and TP1
+decode batches, sampled rows of the chunked-prefill score matrix), and the
+edge cases of "Deterministic sparse top-k" (PR 54955) and "What is fixed"
+(PR 51538): heavy ties, signed zeros, NaN and -inf, negative and oversized
+lengths, offsets that break 16-byte alignment, rows shorter than, equal to
+and one longer than k, and empty batches.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import ensure_built
+from synthetic import workload_case
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def ds():
+    return ensure_built()
+
+
+def run(ds, scores, starts, ends, k):
+    s = torch.as_tensor(scores, dtype=torch.float32).to(DEV).contiguous()
+    a = torch.as_tensor(starts, dtype=torch.int32).to(DEV)
+    b = torch.as_tensor(ends, dtype=torch.int32).to(DEV)
+    got = ds.topk_per_row(s, a, b, k)
+    torch.cuda.synchronize()
+    return got.cpu().numpy()
+
+
+def check(ds, scores, starts, ends, k):
+    scores = np.asarray(scores, dtype=np.float32)
+    got = run(ds, scores, starts, ends, k)
+    want = oracle.topk_per_row(scores, np.asarray(starts), np.asarray(ends), k)
+    assert np.array_equal(got, want), (
+        f"rows differ: {np.nonzero((got != want).any(1))[0][:10].tolist()}")
+    return got
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "tp2_decode"])
+def test_named_workloads_exact(ds, name):
+    c = workload_case(name, device="cpu")
+    check(ds, c.np_scores(), c.np_int("row_starts"), c.np_int("row_ends"), c.k)
+
+
+def test_tp1_decode_scores_exact(ds):
+    c = workload_case("tp1_fp8_decode", device="cuda")
+    got = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k).cpu().numpy()
+    want = oracle.topk_per_row(c.np_scores(), c.np_int("row_starts"), c.np_int("row_ends"), c.k)
+    assert np.array_equal(got, want)
+
+
+def test_chunked_prefill_scores_sampled(ds):
+    # 4096 x 65536 fp32 scores (1 GiB) on the device; the oracle checks a
+    # seeded sample of rows, the kernel runs on the full matrix.
+    T, ctx = 4096, 65536
+    g = torch.Generator(device="cuda").manual_seed(3)
+    pos = torch.arange(ctx - T, ctx, dtype=torch.int32, device=DEV)
+    scores = torch.randn((T, ctx), generator=g, device=DEV)
+    col = torch.arange(ctx, device=DEV)[None, :]
+    scores = torch.where(col < (pos + 1)[:, None], scores, torch.full_like(scores, float("nan")))
+    starts = torch.zeros(T, dtype=torch.int32, device=DEV)
+    idx = ds.topk_per_row(scores, starts, pos + 1, 2048).cpu().numpy()
+    rows = np.random.default_rng(0).choice(T, 24, replace=False).tolist() + [0, T - 1]
+    sub = scores[rows].cpu().numpy()
+    want = oracle.topk_per_row(sub, np.zeros(len(rows)), (pos + 1).cpu().numpy()[rows], 2048)
+    assert np.array_equal(idx[rows], want)
+    # Properties that hold for every row: ascending, in range, exactly k.
+    assert (idx >= 0).all() and (np.diff(idx, axis=1) > 0).all()
+    assert (idx < (pos + 1).cpu().numpy()[:, None]).all()
+
+
+def test_heavy_ties_integer_scores(ds):
+    rng = np.random.default_rng(1)
+    for L, k in [(100, 10), (5000, 2048), (32768, 2048), (70000, 2048)]:
+        s = rng.integers(0, 8, (3, L)).astype(np.float32)
+        check(ds, s, [0, 0, 0], [L, L, L], k)
+
+
+def test_all_equal_and_two_values(ds):
+    s = np.full((2, 9000), 1.5, dtype=np.float32)
+    s[1, ::3] = 2.5
+    got = check(ds, s, [0, 0], [9000, 9000], 2048)
+    assert got[0].tolist() == list(range(2048))
+
+
+def test_special_values(ds):
+    rng = np.random.default_rng(2)
+    L = 6000
+    s = rng.choice(np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan], np.float32), (4, L))
+    check(ds, s, [0] * 4, [L] * 4, 700)
+    check(ds, s, [0] * 4, [L] * 4, 64)
+    s2 = np.full((1, 3000), np.nan, np.float32)
+    s2[0, 1000:1010] = -np.inf
+    check(ds, s2, [0], [3000], 2048)
+
+
+def test_lengths_clamped_and_padded(ds):
+    rng = np.random.default_rng(3)
+    stride = 5000
+    s = rng.standard_normal((8, stride)).astype(np.float32)
+    starts = [0, 10, 0, 100, 4000, 5000, -3, 7]
+    ends = [-1, 5, 2048, 2149, 9999, 5001, 100, 2056]
+    got = check(ds, s, starts, ends, 2048)
+    assert (got[0] == -1).all() and (got[1] == -1).all() and (got[5] == -1).all()
+    assert got[2].tolist() == list(range(2048))
+    assert (got[4][1000:] == -1).all()
+
+
+def test_k_boundaries(ds):
+    rng = np.random.default_rng(4)
+    for k in [1, 2, 63, 64, 2047, 2048, 2049, 4096]:
+        for L in [k - 1, k, k + 1, 3 * k + 5]:
+            if L <= 0:
+                continue
+            s = np.round(rng.standard_normal((2, L)) * 8).astype(np.float32) / 8
+            check(ds, s, [0, 0], [L, L], k)
+
+
+def test_unaligned_offsets_and_strides(ds):
+    rng = np.random.default_rng(5)
+    for stride in [4097, 10001]:
+        s = (np.round(rng.standard_normal((6, stride)) * 4) / 4).astype(np.float32)
+        starts = [1, 2, 3, 5, 0, 17]
+        ends = [stride, stride - 1, 4000, stride, 3001, 9000]
+        check(ds, s, starts, ends, 512)
+
+
+def test_offset_invariance(ds):
+    rng = np.random.default_rng(6)
+    base = (np.round(rng.standard_normal(20000) * 8) / 8).astype(np.float32)
+    ref = run(ds, base[None], [0], [20000], 2048)[0]
+    for off in [1, 3, 64, 1000]:
+        s = np.full((1, 20000 + off), np.nan, np.float32)
+        s[0, off:] = base
+        assert np.array_equal(run(ds, s, [off], [20000 + off], 2048)[0], ref)
+
+
+def test_batch_invariance_of_indices(ds):
+    from synthetic import invariance_batch
+    ref = None
+    for B in [1, 7, 64, 256]:
+        slot = (B * 5) // 7
+        c = invariance_batch(B, slot, device="cuda")
+        idx = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)[slot].cpu().numpy()
+        if ref is None:
+            ref = idx
+            want = oracle.topk_per_row(c.scores[slot:slot + 1].cpu().numpy(), [0],
+                                       [c.meta["ctx"][slot]], c.k)[0]
+            assert np.array_equal(ref, want)
+        assert np.array_equal(idx, ref), B
+
+
+def test_empty_batch(ds):
+    s = torch.zeros((0, 128), dtype=torch.float32, device=DEV)
+    z = torch.zeros(0, dtype=torch.int32, device=DEV)
+    assert ds.topk_per_row(s, z, z, 16).shape == (0, 16)
+
+
+def test_run_to_run_deterministic(ds):
+    c = workload_case("tp2_decode", device="cuda")
+    a = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)
+    b = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)
+    assert torch.equal(a, b)
