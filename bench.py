@@ -1,0 +1,516 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse-MLA decode hot path on GB300.
+
+One step = one pass of the whole path over one decode batch: the
+deterministic top-k over the indexer scores, then sparse MLA attention
+(split kernel + fixed-order combine) over the selected entries of the paged
+latent KV cache. Workload: the TP2-shaped decode batch (32 requests, 64
+heads, contexts uniform in [4096, 32768], top-k 2048, bf16 latent KV in
+64-entry pages, d_qk 576, d_v 512), seeded synthetic data.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0. `value` is decode tokens/s of the whole job
+(one token = one request row per step, all heads), measured with CUDA events
+around K steps replayed from a CUDA graph, inputs resident in HBM. Four
+independent input sets rotate so the gathered KV (4 x 75.5 MB) exceeds the
+129 MB L2 between reuses. `e2e` repeats the step through the public API with
+pinned host buffers: the step's inputs are copied host->device, and out, lse
+and idx are read back, inside the timed region. Under torchrun every rank
+runs its own batch (rows are independent: weak scaling, no collective on the
+data path).
+
+`--impl reference` times the CPU oracle (test infrastructure, the
+reference arm of this comparison) on bounded samples of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "tp2_decode"
+WORKLOAD_DESC = ("TP2-shaped sparse MLA decode: batch 32, 64 heads, contexts uniform int in "
+                 "[4096, 32768], topk 2048, bf16 paged latent KV (page 64, random block-table "
+                 "permutation), d_qk 576 (512+64), d_v 512, fp32 N(0,1) scores, scale 1/sqrt(576)")
+METRIC = "sparse-MLA decode tokens/s and top-k rows/s on 1 GB300; % of roofline"
+N_SETS = 4
+HBM_CONTRACT_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=400)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sets", type=int, default=N_SETS,
+                    help="rotating input sets (profiling runs use 1 to stay small)")
+    return ap.parse_args()
+
+
+def dist_setup(n_gpus):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def max_over_ranks(x, world):
+    """Max of a float over ranks (the job finishes when the slowest does)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "invariant_sparse_mla_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        if t.get("source_sha") == kernel_source_sha():
+            return t
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.gpu_id is not None:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.5)   # nvidia-smi start-up
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, smax, reasons = [], None, set()
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1 + 0.06):
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for_smi(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local < len(ids):
+            return ids[local]
+    return local
+
+
+def algorithmic_bytes(case, idx):
+    """Bytes the path must move at minimum (no re-reads, no workspaces).
+
+    top-k: every in-range score read once (4 B) + idx written (4 B each).
+    attention: every valid selected KV row read once (1152 B bf16) + q read
+    + out (bf16) and lse written + idx read.
+    """
+    import torch
+    L = (case.row_ends - case.row_starts).clamp(min=0).to(torch.int64)
+    topk = 4 * int(L.sum()) + 4 * idx.numel()
+    valid = int((idx >= 0).sum())
+    R, H = case.q.shape[0], case.q.shape[1]
+    attn = valid * 1152 + case.q.numel() * 2 + R * H * 512 * 2 + R * H * 4 + idx.numel() * 4
+    flops = 2 * valid * H * (576 + 512)
+    return topk, attn, flops
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import invariant_sparse_mla_gb300 as ds
+    from synthetic import workload_case
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sets = []
+    n_sets = args.sets
+    for s in range(n_sets):
+        c = workload_case(WORKLOAD, device="cuda")
+        if s > 0 or rank > 0:
+            # Independent batches: reseed by regenerating with a shifted seed.
+            from synthetic import WORKLOADS, decode_case, _uniform_ints
+            w = WORKLOADS[WORKLOAD]
+            seed = w["seed"] + 1000 * rank + 17 * s
+            ctx = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], seed)
+            c = decode_case(WORKLOAD, ctx, w["H"], w["k"], w["kv"], seed, w["scores"],
+                            stride=w["stride"], device="cuda")
+        R, H, k = c.q.shape[0], c.H, c.k
+        c.idx = torch.empty((R, k), dtype=torch.int32, device=dev)
+        c.out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
+        c.lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+        c.ws = torch.empty(ds.attention_workspace_size(R, H, k), dtype=torch.uint8, device=dev)
+        sets.append(c)
+    R, H, k = sets[0].q.shape[0], sets[0].H, sets[0].k
+    stream = torch.cuda.Stream(device=dev)
+
+    def topk(c):
+        ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k, idx_out=c.idx, stream=stream)
+
+    def decode(c):
+        ds.sparse_mla_decode(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.idx, c.lens, c.scale,
+                             out=c.out, lse=c.lse, workspace=c.ws, stream=stream)
+
+    def step(c):
+        topk(c)
+        decode(c)
+
+    # Warm up eagerly (also resolves lazy module loading), then capture graphs.
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for c in sets:
+                step(c)
+    stream.synchronize()
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in sets:
+                fn(c)
+        return g
+
+    g_step, g_topk, g_dec = capture(step), capture(topk), capture(decode)
+    reps = max(1, math.ceil(args.steps / n_sets))
+    steps = reps * n_sets
+    wreps = max(1, math.ceil(max(args.warmup, 3) / n_sets))
+
+    def timed(graph, n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):   # replay() launches on the current stream
+            e0.record(stream)
+            for _ in range(n):
+                graph.replay()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    with torch.cuda.stream(stream):
+        for _ in range(wreps):
+            g_step.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_id_for_smi(local))
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    secs = timed(g_step, reps)
+    t1 = time.time()
+    barrier(world)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    secs = max_over_ranks(secs, world)
+
+    # Per-kernel averages (graphs of one call per input set).
+    n_k = max(8, min(500, reps))
+    topk_s = timed(g_topk, n_k) / (n_k * n_sets)
+    dec_s = timed(g_dec, n_k) / (n_k * n_sets)
+
+    # Work per step (mean over the input sets).
+    tb, ab, fl = zip(*[algorithmic_bytes(c, c.idx) for c in sets])
+    topk_bytes, attn_bytes, attn_flops = (sum(tb) / n_sets, sum(ab) / n_sets, sum(fl) / n_sets)
+
+    # End to end through the public API with pinned host buffers.
+    e2e = None if args.no_e2e else run_e2e(ds, sets, stream, dev,
+                                           steps_e2e=max(20, min(400, args.steps // 50)),
+                                           world=world)
+
+    hbm, tflops, peak_kind = load_peaks()
+    value = world * R * steps / secs
+    ms_per_step = secs / steps * 1e3
+    launches = steps * 3  # top-k + split + combine
+    attn_gbs = attn_bytes / dec_s / 1e9
+    topk_gbs = topk_bytes / topk_s / 1e9
+    roof_s = max(attn_bytes / (HBM_CONTRACT_GBS * 1e9), attn_flops / (tflops * 1e12))
+    traffic = ncu_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": wreps * n_sets,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; random-init latent KV, N(0,1) scores)",
+        "config": {"workload": WORKLOAD_DESC, "global_batch": R * world, "heads": H, "topk": k,
+                   "parallelism": f"replicas x{world} (rows independent, no collective)",
+                   "l2": f"{n_sets} rotating input sets, {n_sets * attn_bytes / 1e6:.0f} MB of "
+                         f"gathered KV vs 129 MB L2", "cuda_graph": True},
+        "topk_rows_per_s": round(world * R / topk_s, 1),
+        "decode_tokens_per_s": round(world * R / dec_s, 1),
+        "topk_us": round(topk_s * 1e6, 3),
+        "decode_us": round(dec_s * 1e6, 3),
+        "roofline": {"bound": "hbm", "kernel": "sparse_mla_decode (split + combine)",
+                     "achieved": round(attn_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(attn_gbs / hbm, 4), "peak_kind": f"{peak_kind} HBM copy",
+                     "traffic": (round(traffic["bytes_per_launch"]) if traffic else None),
+                     "algorithmic_bytes": round(attn_bytes),
+                     "frac_of_contract_roofline": round(roof_s / dec_s, 4)},
+        "roofline_topk": {"bound": "hbm", "achieved": round(topk_gbs, 1), "peak": hbm,
+                          "unit": "GB/s", "frac": round(topk_gbs / hbm, 4),
+                          "algorithmic_bytes": round(topk_bytes)},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(sets[0], budget_s=10.0)
+    return line
+
+
+def run_e2e(ds, sets, stream, dev, steps_e2e, world):
+    """Host -> device inputs, the two calls, device -> host results, per step."""
+    import torch
+    host = []
+    for c in sets:
+        h = {name: getattr(c, name).cpu().pin_memory()
+             for name in ("scores", "row_starts", "row_ends", "q", "block_table", "lens")}
+        h["idx"] = torch.empty_like(c.idx, device="cpu").pin_memory()
+        h["out"] = torch.empty_like(c.out, device="cpu").pin_memory()
+        h["lse"] = torch.empty_like(c.lse, device="cpu").pin_memory()
+        host.append(h)
+    dbufs = [{name: getattr(c, name).clone() for name in
+              ("scores", "row_starts", "row_ends", "q", "block_table", "lens")} for c in sets]
+    h2d = sum(host[0][n].numel() * host[0][n].element_size()
+              for n in ("scores", "row_starts", "row_ends", "q", "block_table", "lens"))
+    d2h = sum(host[0][n].numel() * host[0][n].element_size() for n in ("idx", "out", "lse"))
+
+    def one(i):
+        c, h, d = sets[i % len(sets)], host[i % len(sets)], dbufs[i % len(sets)]
+        with torch.cuda.stream(stream):
+            for n in d:
+                d[n].copy_(h[n], non_blocking=True)
+            ds.topk_per_row(d["scores"], d["row_starts"], d["row_ends"], c.k, idx_out=c.idx,
+                            stream=stream)
+            ds.sparse_mla_decode(d["q"], c.kv_pages, c.kv_dtype, d["block_table"], c.idx,
+                                 d["lens"], c.scale, out=c.out, lse=c.lse, workspace=c.ws,
+                                 stream=stream)
+            h["idx"].copy_(c.idx, non_blocking=True)
+            h["out"].copy_(c.out, non_blocking=True)
+            h["lse"].copy_(c.lse, non_blocking=True)
+        stream.synchronize()   # the caller reads the result
+
+    for i in range(8):
+        one(i)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps_e2e):
+        one(i)
+    e1.record(stream)
+    e1.synchronize()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    R = sets[0].q.shape[0]
+    return {"value": round(world * R * steps_e2e / secs, 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps_e2e,
+            "kv_cache": "resident on the device (serving state, not a per-step input)"}
+
+
+def oracle_sample_inputs(case, rows):
+    """Host copies of what the oracle needs for `rows` of a decode batch."""
+    import numpy as np
+    import torch
+    scores = case.scores[rows].cpu().numpy()
+    starts = case.row_starts.cpu().numpy()[rows]
+    ends = case.row_ends.cpu().numpy()[rows]
+    bt = case.block_table.cpu().numpy()[rows]
+    q = case.q[rows].cpu().view(torch.int16).numpy().view(np.uint16)
+    used = np.unique(bt[bt >= 0])
+    remap = np.zeros(int(used.max()) + 1 if used.size else 1, dtype=np.int64)
+    remap[used] = np.arange(used.size)
+    kv = case.kv_pages.index_select(0, torch.as_tensor(used, device=case.kv_pages.device))
+    kv = kv.cpu().view(torch.int16).numpy().view(np.uint16)
+    bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1)
+    lens = case.lens.cpu().numpy()[rows]
+    return scores, starts, ends, q, kv, bt2, lens
+
+
+def oracle_step(inputs, k, scale, heads=None):
+    import oracle
+    scores, starts, ends, q, kv, bt, lens = inputs
+    idx = oracle.topk_per_row(scores, starts, ends, k)
+    if heads is not None:
+        q = q[:, heads]
+    return oracle.sparse_mla_decode(q, kv, "bf16", bt, idx, lens, scale)
+
+
+def cpu_baseline(case, budget_s):
+    """The oracle on the host cores over a bounded sample of the workload:
+    decode rows of one input set, cycled until `budget_s` of oracle time."""
+    cores = len(os.sched_getaffinity(0))
+    R = case.q.shape[0]
+    cache = {}
+    done, t_used = 0, 0.0
+    while t_used < budget_s and done < 100000:
+        r = done % R
+        if r not in cache:
+            cache[r] = oracle_sample_inputs(case, [r])
+        t0 = time.perf_counter()
+        oracle_step(cache[r], case.k, case.scale)
+        t_used += time.perf_counter() - t0
+        done += 1
+    return {"value": round(done / t_used, 3), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{done} decode-row computations (the {R} rows of input set 0, cycled; "
+                      f"top-k + float64 attention over all heads), {t_used:.1f} s of oracle "
+                      f"time; numpy BLAS may use all {cores} host cores"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, one decode row of the batch per step."""
+    if rank != 0:
+        return None
+    from synthetic import workload_case
+    case = workload_case(WORKLOAD, device="cpu")
+    R, H = case.q.shape[0], case.H
+    cores = len(os.sched_getaffinity(0))
+    cache = {}
+    t_used, n = 0.0, 0
+    cap_s = 120.0   # bounds the run when --steps is large
+    for i in range(args.warmup + args.steps):
+        r = i % R
+        if r not in cache:
+            cache[r] = oracle_sample_inputs(case, [r])
+        t0 = time.perf_counter()
+        oracle_step(cache[r], case.k, case.scale)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            t_used += dt
+            n += 1
+            if t_used > cap_s:
+                break
+    value = n / t_used
+    sample = (f"{n} timed steps, each one decode row of the {R}-row batch (rows cycled): "
+              f"top-k + float64 attention over all {H} heads, {t_used:.1f} s")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": n, "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_used / max(n, 1) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": WORKLOAD_DESC, "global_batch": R,
+                       "parallelism": "CPU oracle, rank 0"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

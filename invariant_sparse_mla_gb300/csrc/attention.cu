@@ -52,11 +52,12 @@ constexpr int kDv = 512;
 constexpr int kRowBytesBf16 = kD * 2;                 // 1152
 constexpr int kRowBytesFp8 = 656;
 constexpr int kChunks = kRowBytesBf16 / 16;           // 72 16-byte chunks per bf16 row
-constexpr int kTile = kTileEntries;                   // 64
-constexpr int kStageBytes = kTile * kRowBytesBf16;    // 73728
+constexpr int kTile = kTileEntries;                   // 32 entries per tile
+constexpr int kStages = 4;                            // KV tile ring
+constexpr int kStageBytes = kTile * kRowBytesBf16;    // 36864
 constexpr int kAtomStride = kTile * 128;              // bytes between 64-dim column blocks
 constexpr int kThreads = 288;                         // 9 warps
-constexpr int kSCols = 64;                            // TMEM columns of one S buffer
+constexpr int kSCols = kTile;                         // TMEM columns of one S buffer
 constexpr int kOCol = 2 * kSCols;                     // first TMEM column of O^T
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 
@@ -67,25 +68,32 @@ template <int HG>
 struct Layout {
   static constexpr int kQBytes = HG * kRowBytesBf16;
   static constexpr int kQ = 0;
-  static constexpr int kKV0 = kQ + kQBytes;
-  static constexpr int kKV1 = kKV0 + kStageBytes;
-  static constexpr int kP = kKV1 + kStageBytes;
+  static constexpr int kKV = kQ + kQBytes;                    // kStages x kStageBytes
+  static constexpr int kP = kKV + kStages * kStageBytes;      // HG rows x 128 B: two P tiles
   static constexpr int kPBytes = HG * 128;
-  static constexpr int kMisc = kP + kPBytes;
-  // misc: barriers, valid masks, alphas, tmem address
-  static constexpr int kBars = kMisc;                         // 16 x u64 reserved
-  static constexpr int kMask = kBars + 16 * 8;                 // kSplitTiles x u64
-  static constexpr int kAlpha = kMask + kSplitTiles * 8;       // 2 x 64 floats
-  static constexpr int kTmemSlot = kAlpha + 2 * 64 * 4;        // u32
-  static constexpr int kNeff = kTmemSlot + 4;                  // int
+  static constexpr int kBars = kP + kPBytes;                  // 24 x u64
+  static constexpr int kMask = kBars + 24 * 8;                // kSplitTiles x u32
+  static constexpr int kAlpha = kMask + kSplitTiles * 4;      // 2 x 64 floats
+  static constexpr int kTmemSlot = kAlpha + 2 * 64 * 4;       // u32
+  static constexpr int kNeff = kTmemSlot + 4;                 // int
   static constexpr int kEnd = kNeff + 12;
-  static constexpr int kSmemBytes = kEnd + 1024;               // + alignment slack
+  static constexpr int kSmemBytes = kEnd + 1024;              // + alignment slack
   static constexpr uint32_t kTmemCols = (kOCol + 4 * HG) <= 256 ? 256u : 512u;
 };
 
-// Barrier slots in the misc area.
-enum Bar { kQFull = 0, kKvFull0 = 1, kKvFull1 = 2, kKvEmpty0 = 3, kKvEmpty1 = 4,
-           kSFull0 = 5, kSFull1 = 6, kPFull = 7, kPvDone = 8, kMmaDone = 9, kNumBars = 10 };
+// Barrier slots. Every barrier that is waited on by parity is only ever
+// waited on for a phase that cannot be overtaken by the next one (each has
+// one in-flight use at a time), so the parity test is unambiguous.
+enum Bar {
+  kQFull = 0,
+  kKvFull = 1,     // 4: producer threads -> MMA (tile landed)
+  kKvEmpty = 5,    // 4: MMA commit -> producers (stage free)
+  kSFull = 9,      // 2: MMA commit -> softmax (S ready)
+  kPFull = 11,     // 2: softmax threads -> MMA (P written)
+  kPvDone = 13,    // 2: MMA commit -> softmax (PV of a tile done)
+  kMmaDone = 15,
+  kNumBars = 16
+};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kBars);
-  uint64_t* vmask = reinterpret_cast<uint64_t*>(smem + LY::kMask);
+  uint32_t* vmask = reinterpret_cast<uint32_t*>(smem + LY::kMask);
   float* alpha_s = reinterpret_cast<float*>(smem + LY::kAlpha);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kTmemSlot);
   int* neff_s = reinterpret_cast<int*>(smem + LY::kNeff);
@@ -173,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const bool producer = warp >= 4 && warp < 8;
+  const int pw = warp - 4;          // producer warp 0..3: rows 8*pw .. 8*pw+7 of every tile
 
   int64_t bid = blockIdx.x;
   const int hg = (int)(bid % p.num_hg);
@@ -191,23 +201,43 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
 
   const int j0 = split * kSplitEntries;
   const int j1 = min(p.k, j0 + kSplitEntries);
+  const int ntiles = (j1 - j0) / kTile;
   const int32_t* idx_row = p.idx + row * (int64_t)p.k;
+  const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
 
-  // Number of tiles up to the last entry that is not -1 padding.
+  // ---- prologue 1: Q copies start; producers read this split's idx entries.
+  // Producer warp pw owns the tiles t = pw + 4i (always stage pw of the ring);
+  // lane l owns row l of each of them.
+  int pos[4] = {-1, -1, -1, -1};
   if (tid == 0) *neff_s = 0;
   __syncthreads();
-  {
-    int last = -1;
-    for (int j = j0 + tid; j < j1; j += kThreads)
-      if (idx_row[j] != -1) last = j;
-    if (last >= 0) atomicMax(neff_s, (last - j0) / kTile + 1);
+  if (producer) {
+    const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
+    const int ptid = tid - 128;
+    for (int c = ptid; c < HG * kChunks; c += 128) {
+      const int h = c / kChunks, ch = c - h * kChunks;
+      cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
+    }
+    cp_async_commit();
+    int last = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = pw + 4 * i;
+      if (t < ntiles) {
+        pos[i] = idx_row[j0 + t * kTile + lane];
+        if (pos[i] != -1) last = t + 1;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    if (lane == 0 && last > 0) atomicMax(neff_s, last);
   }
   __syncthreads();
   const int n_eff = row_ok ? *neff_s : 0;
-  const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
 
   if (!row_ok && tid == 0 && p.err != nullptr) atomicOr(p.err, kErrRowReq);
   if (n_eff == 0) {  // nothing to attend to in this split
+    if (producer) cp_async_wait_all();  // Q copies must land before the CTA exits
     if (tid < HG) {
       p.part_m[part_base + tid] = -INFINITY;
       p.part_l[part_base + tid] = 0.0f;
@@ -215,12 +245,47 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
     return;
   }
 
+  // ---- prologue 2: page lookups and validity masks; barriers; TMEM.
+  int64_t grow[4] = {-1, -1, -1, -1};   // global KV row of each owned entry, -1 = skip
+  if (producer) {
+    int err_bits = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = pw + 4 * i;
+      bool valid = false;
+      if (t < n_eff) {
+        const int ps = pos[i];
+        if (ps >= 0 && (int64_t)ps < len) {
+          const int64_t blk = ps >> 6;
+          if (blk < p.bt_stride) {
+            const int64_t page = p.block_table[bt_row * p.bt_stride + blk];
+            if (page >= 0 && page < p.num_pages) {
+              grow[i] = page * 64 + (ps & 63);
+              valid = true;
+            } else {
+              err_bits |= kErrPage;
+            }
+          } else {
+            err_bits |= kErrPage;
+          }
+        } else if (ps != -1) {
+          err_bits |= kErrIdx;
+        }
+      }
+      const uint32_t ballot = __ballot_sync(0xffffffffu, valid);
+      if (lane == 0 && t < kSplitTiles) vmask[t] = ballot;
+    }
+    if (err_bits && p.err != nullptr) atomicOr(p.err, err_bits);
+  }
   if (tid == 0) {
-    // 128-count barriers take one arrival per producer (or softmax) thread;
-    // the others one tcgen05.commit.
     for (int i = 0; i < kNumBars; ++i) {
-      const bool per_thread = i == kQFull || i == kKvFull0 || i == kKvFull1 || i == kPFull;
-      mbar_init(&bars[i], per_thread ? 128u : 1u);
+      // q_full and p_full take one arrival per producer / softmax thread,
+      // kv_full one per lane of the warp that owns the stage, the rest one
+      // tcgen05.commit.
+      uint32_t count = 1u;
+      if (i == kQFull || i == kPFull || i == kPFull + 1) count = 128u;
+      if (i >= kKvFull && i < kKvFull + kStages) count = 32u;
+      mbar_init(&bars[i], count);
     }
     mbar_fence_init();
   }
@@ -232,179 +297,155 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  uint64_t* pv_done = &bars[kPvDone];
-  uint64_t* mma_done = &bars[kMmaDone];
 
   bool failed = false;
 
-  if (warp >= 4 && warp < 8) {
+  if (producer) {
     // ------------------------------------------------------------ producers
-    const int ptid = tid - 128;
-    const int pw = warp - 4;
-    // Q rows of this head group.
-    const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
-    for (int c = ptid; c < HG * kChunks; c += 128) {
-      const int h = c / kChunks, ch = c - h * kChunks;
-      cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
-    }
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    mbar_arrive(&bars[kQFull]);
-
-    int err_bits = 0;
-    for (int t = 0; t < n_eff && !failed; ++t) {
-      const int stage = t & 1;
-      // The warp decides together, so its shuffles below never diverge.
-      const bool ok = t < 2 || mbar_wait(&bars[kKvEmpty0 + stage], ((t >> 1) - 1) & 1);
+    // Warp pw fills stage pw with tiles pw, pw+4, ...: it waits for its own
+    // copies (or stores) to land, fences them for the tensor core and
+    // arrives; the four warps keep four tiles in flight.
+    const uint32_t stage_base = sbase + LY::kKV + pw * kStageBytes;
+    bool q_signalled = false;
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i) {
+      const int t = pw + 4 * i;
+      if (t >= n_eff) break;
+      const int64_t gi = i == 0 ? grow[0] : i == 1 ? grow[1] : i == 2 ? grow[2] : grow[3];
+      const bool ok = i == 0 || mbar_wait(&bars[kKvEmpty + pw], (i - 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         failed = true;
         break;
       }
-      // Row lookup: lane r (< 16) resolves tile row 16*pw + r.
-      const int r = lane & 15;
-      const int j = j0 + t * kTile + pw * 16 + r;
-      const int pos = idx_row[j];
-      bool valid = pos >= 0 && (int64_t)pos < len;
-      int64_t grow = -1;
-      if (valid) {
-        const int64_t blk = pos >> 6;
-        if (blk < p.bt_stride) {
-          const int64_t page = p.block_table[bt_row * p.bt_stride + blk];
-          if (page >= 0 && page < p.num_pages) {
-            grow = page * 64 + (pos & 63);
-          } else {
-            valid = false;
-            err_bits |= kErrPage;
-          }
-        } else {
-          valid = false;
-          err_bits |= kErrPage;
-        }
-      } else if (pos != -1) {
-        err_bits |= kErrIdx;
-      }
-      const uint32_t ballot = __ballot_sync(0xffffffffu, valid) & 0xFFFFu;
-      if (lane == 0)
-        reinterpret_cast<uint16_t*>(&vmask[t])[pw] = (uint16_t)ballot;
-
-      const uint32_t stage_base = sbase + (stage ? LY::kKV1 : LY::kKV0);
       if constexpr (!FP8) {
-        for (int rr = 0; rr < 16; ++rr) {
-          const int64_t g = __shfl_sync(0xffffffffu, grow, rr);
-          const int tr = pw * 16 + rr;
+#pragma unroll 4
+        for (int rr = 0; rr < kTile; ++rr) {
+          const int64_t g = __shfl_sync(0xffffffffu, gi, rr);
           const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
 #pragma unroll
-          for (int i = 0; i < 3; ++i) {
-            const int c = lane + 32 * i;
-            if (c < kChunks) cp_async_16(stage_base + swz_off(tr, c, kAtomStride), src + c * 16, nbytes);
+          for (int j = 0; j < 3; ++j) {
+            const int c = lane + 32 * j;
+            if (c < kChunks)
+              cp_async_16(stage_base + swz_off(rr, c, kAtomStride), src + c * 16, nbytes);
           }
         }
         cp_async_commit();
         cp_async_wait_all();
       } else {
-        for (int r0 = 0; r0 < 16; r0 += 4) {
-          uint2 codes[4][2];
-          float scl[4][2];
-          uint4 rope[4];
+        if (i == 0) cp_async_wait_all();   // Q
+#pragma unroll 1
+        for (int r0 = 0; r0 < kTile; r0 += 8) {
+          uint2 codes[8][2];
+          float scl[8][2];
+          uint4 rope[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int64_t g = __shfl_sync(0xffffffffu, grow, r0 + u);
+          for (int u = 0; u < 8; ++u) {
+            const int64_t g = __shfl_sync(0xffffffffu, gi, r0 + u);
             const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesFp8;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int c = lane + 32 * i;  // latent output chunk 0..63
+            for (int j = 0; j < 2; ++j) {
+              const int c = lane + 32 * j;  // latent output chunk 0..63
+              codes[u][j] = make_uint2(0u, 0u);
+              scl[u][j] = 0.0f;
               if (g >= 0) {
-                codes[u][i] = *reinterpret_cast<const uint2*>(src + c * 8);
-                scl[u][i] = *reinterpret_cast<const float*>(src + 512 + (c >> 4) * 4);
-              } else {
-                codes[u][i] = make_uint2(0u, 0u);
-                scl[u][i] = 0.0f;
+                codes[u][j] = *reinterpret_cast<const uint2*>(src + c * 8);
+                scl[u][j] = *reinterpret_cast<const float*>(src + 512 + (c >> 4) * 4);
               }
             }
             rope[u] = make_uint4(0u, 0u, 0u, 0u);
             if (lane < 8 && g >= 0) rope[u] = *reinterpret_cast<const uint4*>(src + 528 + lane * 16);
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int tr = pw * 16 + r0 + u;
+          for (int u = 0; u < 8; ++u) {
+            const int tr = r0 + u;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int c = lane + 32 * i;
+            for (int j = 0; j < 2; ++j) {
+              const int c = lane + 32 * j;
               st_shared_v4(stage_base + swz_off(tr, c, kAtomStride),
-                           dequant8(codes[u][i].x, codes[u][i].y, scl[u][i]));
+                           dequant8(codes[u][j].x, codes[u][j].y, scl[u][j]));
             }
             if (lane < 8) st_shared_v4(stage_base + swz_off(tr, 64 + lane, kAtomStride), rope[u]);
           }
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars[kKvFull0 + stage]);
+      if (!q_signalled) {
+        mbar_arrive(&bars[kQFull]);
+        q_signalled = true;
+      }
+      mbar_arrive(&bars[kKvFull + pw]);
+    }
+    if (!q_signalled && !failed) {   // this warp had no tile: still release Q
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[kQFull]);
     }
     cp_async_wait_all();
-    if (err_bits && p.err != nullptr) atomicOr(p.err, err_bits);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t idesc_qk = make_idesc_bf16(128, kTile, 0, 0);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, HG, 1, 0);
       const uint32_t q_addr = sbase + LY::kQ;
       const uint32_t p_addr = sbase + LY::kP;
       auto issue_pv = [&](int t) {
-        const uint32_t kv_addr = sbase + ((t & 1) ? LY::kKV1 : LY::kKV0);
+        const uint32_t kv_addr = sbase + LY::kKV + (t & (kStages - 1)) * kStageBytes;
+        const uint32_t p_tile = p_addr + (t & 1) * (kTile * 2);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint64_t a = make_sw128_desc(kv_addr + 2 * b * kAtomStride + kk * 2048,
                                                kAtomStride, 1024);
-            const uint64_t bd = make_sw128_desc(p_addr + kk * 32, 16, 1024);
+            const uint64_t bd = make_sw128_desc(p_tile + kk * 32, 16, 1024);
             mma_bf16_ss(tmem + kOCol + b * HG, a, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
           }
         }
       };
       if (!mbar_wait(&bars[kQFull], 0)) failed = true;
       for (int t = 0; t < n_eff && !failed; ++t) {
-        const int stage = t & 1;
-        if (!mbar_wait(&bars[kKvFull0 + stage], (t >> 1) & 1)) {
+        const int stage = t & (kStages - 1);
+        if (!mbar_wait(&bars[kKvFull + stage], (t / kStages) & 1)) {
           failed = true;
           break;
         }
         tc_fence_after();
-        const uint32_t kv_addr = sbase + (stage ? LY::kKV1 : LY::kKV0);
+        const uint32_t kv_addr = sbase + LY::kKV + stage * kStageBytes;
 #pragma unroll 4
         for (int kk = 0; kk < kD / 16; ++kk) {
           const int ka = kk >> 2;
           const uint32_t off = (kk & 3) * 32;
           const uint64_t a = make_sw128_desc(q_addr + ka * (HG * 128) + off, 16, 1024);
           const uint64_t b = make_sw128_desc(kv_addr + ka * kAtomStride + off, 16, 1024);
-          mma_bf16_ss(tmem + stage * kSCols, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + (t & 1) * kSCols, a, b, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars[kSFull0 + stage]);
+        mma_commit(&bars[kSFull + (t & 1)]);
         if (t >= 1) {
-          if (!mbar_wait(&bars[kPFull], (t - 1) & 1)) {
+          const int u = t - 1;
+          if (!mbar_wait(&bars[kPFull + (u & 1)], (u >> 1) & 1)) {
             failed = true;
             break;
           }
           tc_fence_after();
-          issue_pv(t - 1);
-          mma_commit(&bars[kKvEmpty0 + ((t - 1) & 1)]);
-          mma_commit(pv_done);
+          issue_pv(u);
+          mma_commit(&bars[kKvEmpty + (u & (kStages - 1))]);
+          mma_commit(&bars[kPvDone + (u & 1)]);
         }
       }
       if (!failed) {
-        if (mbar_wait(&bars[kPFull], (n_eff - 1) & 1)) {
+        const int u = n_eff - 1;
+        if (mbar_wait(&bars[kPFull + (u & 1)], (u >> 1) & 1)) {
           tc_fence_after();
-          issue_pv(n_eff - 1);
-          mma_commit(pv_done);
+          issue_pv(u);
+          mma_commit(&bars[kPvDone + (u & 1)]);
         } else {
           failed = true;
         }
       }
       // Drain: wait until every MMA issued above has completed.
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0);
+      mma_commit(&bars[kMmaDone]);
+      mbar_wait(&bars[kMmaDone], 0);
     }
     __syncwarp();
   } else {
@@ -419,18 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
     // timeout decision is made jointly: either all leave the loop or none.
     for (int t = 0; t < n_eff; ++t) {
       const int sb = t & 1;
-      const bool ok = mbar_wait(&bars[kSFull0 + sb], (t >> 1) & 1);
+      const bool ok = mbar_wait(&bars[kSFull + sb], (t >> 1) & 1);
       bool need = false;
       if (ok) {
         tc_fence_after();
         if (warp_has_heads) {
           tmem_ld32_sync(tmem + lane_base + sb * kSCols, s);
-          tmem_ld32_sync(tmem + lane_base + sb * kSCols + 32, s + 32);
-          const uint64_t mask = vmask[t];
+          const uint32_t mask = vmask[t];
           float mt = -INFINITY;
 #pragma unroll
           for (int j = 0; j < kSCols; ++j) {
-            s[j] = ((mask >> j) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
+            s[j] = ((mask >> j) & 1u) ? s[j] * p.scale_log2 : -INFINITY;
             mt = fmaxf(mt, s[j]);
           }
           float a = 1.0f;
@@ -448,7 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
         break;
       }
       const bool any = named_bar_or(2, 128, need);
-      const bool ok2 = t == 0 || mbar_wait(pv_done, (t - 1) & 1);
+      // Rescaling O^T needs PV(t-1) complete; reusing P buffer t&1 needs PV(t-2).
+      bool ok2 = true;
+      if (any) ok2 = mbar_wait(&bars[kPvDone + ((t - 1) & 1)], ((t - 1) >> 1) & 1);
+      else if (t >= 2) ok2 = mbar_wait(&bars[kPvDone + (t & 1)], ((t >> 1) - 1) & 1);
       if (named_bar_or(3, 128, !ok2)) {
         failed = true;
         break;
@@ -473,28 +516,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       if (warp_has_heads && h < HG) {
         float lsum = 0.0f;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int c4 = 0; c4 < kTile / 8; ++c4) {
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float p0 = (m == -INFINITY) ? 0.0f : ex2(s[8 * c8 + 2 * i] - m);
-            const float p1 = (m == -INFINITY) ? 0.0f : ex2(s[8 * c8 + 2 * i + 1] - m);
+            const float p0 = (m == -INFINITY) ? 0.0f : ex2(s[8 * c4 + 2 * i] - m);
+            const float p1 = (m == -INFINITY) ? 0.0f : ex2(s[8 * c4 + 2 * i + 1] - m);
             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
             const float2 pr = __bfloat1622float2(pb);
             lsum += pr.x;
             lsum += pr.y;
             w[i] = *reinterpret_cast<const uint32_t*>(&pb);
           }
-          const uint32_t dst = smem_u32(prow) + ((c8 ^ (h & 7)) << 4);
-          st_shared_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+          const int c = sb * (kTile / 8) + c4;   // 16-byte chunk within the 128-byte row
+          st_shared_v4(smem_u32(prow) + ((c ^ (h & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
         }
         l += lsum;
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars[kPFull]);
+      mbar_arrive(&bars[kPFull + sb]);
     }
-    if (!failed && !mbar_wait(pv_done, (n_eff - 1) & 1)) failed = true;
+    const int u = n_eff - 1;
+    if (!failed && !mbar_wait(&bars[kPvDone + (u & 1)], (u >> 1) & 1)) failed = true;
     if (!failed) {
       tc_fence_after();
       // Epilogue: partial O (unnormalised, relative to m), m and l.

@@ -12,12 +12,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -48,15 +42,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete. Gives up after
-// `limit_ns` nanoseconds and returns false; the caller then records the
-// timeout and winds the kernel down instead of spinning forever.
+// about `limit_cycles` SM clock cycles (2^32, i.e. about 2 s) and returns
+// false; the caller then records the timeout and winds the kernel down
+// instead of spinning forever. The clock is read only every 256 polls so the
+// poll loop reacts to the phase flip without extra latency.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          uint64_t limit_cycles = 1ull << 32) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
+  const uint64_t t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > limit_ns) return false;
+    if ((it & 255u) == 0u && (uint64_t)(clock64() - t0) > limit_cycles) return false;
   }
 }
 

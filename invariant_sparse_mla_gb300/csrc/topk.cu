@@ -28,6 +28,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "internal.h"
 
 namespace dsmla {
@@ -216,13 +218,323 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Cluster variant: the row is cut into C contiguous chunks, one per CTA of a
+// thread-block cluster (C <= 8). Each CTA keeps its chunk's keys in shared
+// memory, so the row is read from HBM exactly once. The per-CTA digit
+// histograms are summed through distributed shared memory after a hardware
+// cluster barrier (every CTA of a cluster is co-scheduled, so the barrier
+// cannot wait on a CTA that never runs); every CTA then derives the same
+// threshold. Histograms are double buffered, so one cluster barrier per digit
+// pass suffices. The compaction counts (greater, equal) per warp with
+// ballots, exchanges the per-CTA totals through distributed shared memory to
+// get each chunk's carry-in, and writes the output in ascending order.
+
+constexpr int kMaxChunk = 16384;       // keys per CTA (64 KiB of shared memory)
+constexpr int kMaxCluster = 8;
+
+// Reads of another CTA's shared memory. They are only issued after a cluster
+// barrier that orders the writes, so they need no memory clobber and may be
+// overlapped freely.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local_ptr, uint32_t rank) {
+  uint32_t remote;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;"
+      : "=r"(remote)
+      : "r"((uint32_t)__cvta_generic_to_shared(local_ptr)), "r"(rank));
+  return remote;
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld(const uint32_t* local_ptr, uint32_t rank) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(dsmem_addr(local_ptr, rank)));
+  return v;
+}
+
+__device__ __forceinline__ uint4 dsmem_ld4(const uint32_t* local_ptr, uint32_t rank) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(dsmem_addr(local_ptr, rank)));
+  return v;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
+    const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ starts,
+    const int32_t* __restrict__ ends, int k, int32_t* __restrict__ out) {
+  extern __shared__ __align__(16) uint32_t keys[];  // this CTA's chunk
+  __shared__ __align__(16) uint32_t hist[2][kBins];
+  __shared__ uint32_t scan_buf[32];
+  __shared__ uint32_t pick[3];
+  __shared__ uint32_t wcount[kWarps][2];        // per-warp (greater, equal) counts
+  __shared__ uint32_t cta_tot[2];               // this CTA's totals, read by later ranks
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t C = cluster_size();
+  const uint32_t crank = cluster_rank();
+  const int64_t row = blockIdx.x / C;
+  const int64_t s = starts[row];
+  const int64_t e = ends[row];
+  int64_t L = 0;
+  if (s >= 0 && s <= stride) {
+    L = e - s;
+    if (L < 0) L = 0;
+    if (L > stride - s) L = stride - s;
+  }
+  int32_t* __restrict__ orow = out + row * (int64_t)k;
+  if (L <= (int64_t)k) {  // uniform over the cluster: no cluster barrier is used
+    if (crank == 0)
+      for (int j = tid; j < k; j += kThreads) orow[j] = (int64_t)j < L ? j : -1;
+    return;
+  }
+
+  // Chunk of this CTA: [c0, c0 + n), chunks a multiple of 4 elements long.
+  const int64_t per = ((L + C - 1) / C + 3) & ~int64_t(3);
+  const int64_t c0 = per * crank;
+  const int n = (int)(c0 >= L ? 0 : (L - c0 < per ? L - c0 : per));
+  const float* __restrict__ p = scores + row * stride + s + c0;
+  const bool aligned = (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
+
+  for (int i = tid; i < kBins; i += kThreads) hist[0][i] = 0u;
+  __syncthreads();
+
+  // Load the chunk (8 x 16 B per thread in flight), store keys, histogram
+  // of the top 11 bits.
+  if (aligned) {
+    const int n4 = n >> 2;
+    const float4* p4 = reinterpret_cast<const float4*>(p);
+    for (int base = 0; base < n4; base += 8 * kThreads) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i < n4) v[u] = p4[i];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i < n4) {
+          uint4 kk;
+          kk.x = score_key(v[u].x);
+          kk.y = score_key(v[u].y);
+          kk.z = score_key(v[u].z);
+          kk.w = score_key(v[u].w);
+          reinterpret_cast<uint4*>(keys)[i] = kk;
+          atomicAdd(&hist[0][kk.x >> 21], 1u);
+          atomicAdd(&hist[0][kk.y >> 21], 1u);
+          atomicAdd(&hist[0][kk.z >> 21], 1u);
+          atomicAdd(&hist[0][kk.w >> 21], 1u);
+        }
+      }
+    }
+    for (int i = (n4 << 2) + tid; i < n; i += kThreads) {
+      const uint32_t kk = score_key(p[i]);
+      keys[i] = kk;
+      atomicAdd(&hist[0][kk >> 21], 1u);
+    }
+  } else {
+    for (int base = 0; base < n; base += 8 * kThreads) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i < n) v[u] = p[i];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i < n) {
+          const uint32_t kk = score_key(v[u]);
+          keys[i] = kk;
+          atomicAdd(&hist[0][kk >> 21], 1u);
+        }
+      }
+    }
+  }
+
+  uint32_t prefix = 0u;
+  int shift = 32;
+  uint32_t take = (uint32_t)k;
+  for (int pass = 0; pass < 3; ++pass) {
+    const int width = pass < 2 ? 11 : 10;
+    const int nshift = shift - width;
+    const uint32_t nbins = 1u << width;
+    const int buf = pass & 1;
+    if (pass > 0) {
+      // hist[buf] was last read by the other CTAs two passes ago, before the
+      // previous pass's cluster barrier.
+      for (int i = tid; i < kBins; i += kThreads) hist[buf][i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t kk = keys[i];
+        if ((kk >> shift) == prefix) atomicAdd(&hist[buf][(kk >> nshift) & (nbins - 1u)], 1u);
+      }
+    }
+    __syncthreads();
+    cluster_sync_all();
+
+    // Cluster-wide counts of this thread's bins (descending bin order): the
+    // thread's four bins are contiguous, so one 16-byte remote load per rank.
+    uint32_t c[kBinsPerThread];
+    uint32_t mine = 0u;
+    const int bhi = (int)nbins - 1 - tid * kBinsPerThread;   // highest of the four
+    {
+      uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+      if (bhi >= kBinsPerThread - 1) {
+        uint4 part[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < (int)C) part[r] = dsmem_ld4(&hist[buf][bhi - 3], (uint32_t)r);
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < (int)C) {
+            acc.x += part[r].x;
+            acc.y += part[r].y;
+            acc.z += part[r].z;
+            acc.w += part[r].w;
+          }
+      }
+      c[0] = acc.w;  // bin bhi
+      c[1] = acc.z;
+      c[2] = acc.y;
+      c[3] = acc.x;  // bin bhi - 3
+      mine = acc.x + acc.y + acc.z + acc.w;
+    }
+    uint32_t total;
+    uint32_t above = block_exclusive_scan(mine, scan_buf, total);
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+      const int b = (int)nbins - 1 - (tid * kBinsPerThread + q);
+      if (b >= 0 && above < take && take <= above + c[q]) {
+        pick[0] = (uint32_t)b;
+        pick[1] = take - above;
+        pick[2] = c[q];
+      }
+      above += c[q];
+    }
+    __syncthreads();
+    const uint32_t b = pick[0];
+    const uint32_t cnt = pick[2];
+    take = pick[1];
+    prefix = (pass == 0 ? 0u : (prefix << width)) | b;
+    shift = nshift;
+    if (cnt == take) break;  // same decision in every CTA of the cluster
+  }
+
+  // Ordered compaction. Warp w owns the contiguous segment [w*seg, w*seg+seg)
+  // of the chunk, read 32 keys at a time.
+  const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int w0 = warp * seg;
+  const int w1 = min(n, w0 + seg);
+  uint32_t ngt = 0u, neq = 0u;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    uint32_t hi = 0u;
+    const bool in = i < w1;
+    if (in) hi = keys[i] >> shift;
+    ngt += __popc(__ballot_sync(0xffffffffu, in && hi > prefix));
+    neq += __popc(__ballot_sync(0xffffffffu, in && hi == prefix));
+  }
+  if (lane == 0) {
+    wcount[warp][0] = ngt;
+    wcount[warp][1] = neq;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t g = 0u, q = 0u;
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t a = wcount[w][0], b2 = wcount[w][1];
+      wcount[w][0] = g;
+      wcount[w][1] = q;
+      g += a;
+      q += b2;
+    }
+    cta_tot[0] = g;
+    cta_tot[1] = q;
+  }
+  __syncthreads();
+  cluster_sync_all();
+  uint32_t carry_gt = 0u, carry_eq = 0u;
+  for (uint32_t r = 0; r < crank; ++r) {
+    carry_gt += dsmem_ld(&cta_tot[0], r);
+    carry_eq += dsmem_ld(&cta_tot[1], r);
+  }
+  uint32_t g = carry_gt + wcount[warp][0];
+  uint32_t qe = carry_eq + wcount[warp][1];
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    uint32_t hi = 0u;
+    const bool in = i < w1;
+    if (in) hi = keys[i] >> shift;
+    const bool is_gt = in && hi > prefix;
+    const bool is_eq = in && hi == prefix;
+    const uint32_t bg = __ballot_sync(0xffffffffu, is_gt);
+    const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t my_g = g + __popc(bg & lt_mask);
+    const uint32_t my_e = qe + __popc(be & lt_mask);
+    if (is_gt) orow[my_g + min(my_e, take)] = (int32_t)(c0 + i);
+    else if (is_eq && my_e < take) orow[my_g + my_e] = (int32_t)(c0 + i);
+    g += __popc(bg);
+    qe += __popc(be);
+  }
+  // No CTA may exit while another can still read its shared memory.
+  cluster_sync_all();
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const int32_t* starts,
                         const int32_t* ends, int k, int32_t* out, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  topk_rows_kernel<<<(unsigned)rows, kThreads, 0, stream>>>(scores, stride, starts, ends, k, out);
-  return cudaGetLastError();
+  // Cluster size from the row stride alone: about 8K keys per CTA, at most 8
+  // CTAs. Rows longer than 8 x 16K keys take the single-CTA kernel.
+  int64_t C = (stride + 8191) / 8192;
+  if (C > kMaxCluster) C = kMaxCluster;
+  const int64_t per = ((stride + C - 1) / C + 3) & ~int64_t(3);
+  if (per > kMaxChunk || rows * C > (int64_t)INT32_MAX) {
+    topk_rows_kernel<<<(unsigned)rows, kThreads, 0, stream>>>(scores, stride, starts, ends, k, out);
+    return cudaGetLastError();
+  }
+  const size_t smem = (size_t)per * sizeof(uint32_t);
+  static std::atomic<bool> attr_set{false};
+  if (!attr_set.load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kMaxChunk * sizeof(uint32_t)));
+    if (e != cudaSuccess) return e;
+    attr_set.store(true, std::memory_order_release);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * C), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, stride, starts, ends, k, out);
 }
 
 }  // namespace dsmla

@@ -244,7 +244,7 @@ def invariance_batch(batch_size, slot, target_seed=0, batch_seed=4, device="cpu"
     t_rows = _normal((target_ctx, D_QK), gt, device).to(torch.bfloat16)
 
     gb = _gen(batch_seed * 1000 + batch_size, device)
-    nb_ctx = torch.randint(1, max_ctx + 1, (batch_size,), generator=gb, device="cpu").tolist()
+    nb_ctx = torch.randint(1, max_ctx + 1, (batch_size,), generator=gb, device=device).tolist()
     ctx = [target_ctx if i == slot else int(nb_ctx[i]) for i in range(batch_size)]
     bt, num_pages = _block_table(ctx, gb, device)
     pool = _kv_pool(num_pages, "bf16", gb, device)
