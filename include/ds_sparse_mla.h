@@ -203,6 +203,33 @@ int ds_sparse_mla_prefill(const void* q, const void* kv_pages, int kv_dtype, int
                           void* out, float* lse, void* workspace, size_t workspace_bytes,
                           int32_t* err_flag, void* stream);
 
+/*
+ * Allocation-free variant of ds_sparse_mla_decode. The pages have no
+ * counterpart to this entry point; it exists for callers that cannot provide
+ * device scratch memory: code running under a memory manager that owns all
+ * device memory, code in the middle of recording a CUDA graph (where a plain
+ * cudaMalloc is not allowed), and loops that cannot afford cudaMalloc's
+ * implicit device synchronisation.
+ *
+ * Arguments, results and errors are those of ds_sparse_mla_decode, minus the
+ * workspace. The scratch is a built-in 32 MiB device array of this library
+ * (each GPU holds it from the time the library's module is first loaded there
+ * until the process exits). Calls whose ds_sparse_mla_workspace_size() exceeds
+ * 32 MiB return DS_ERR_WORKSPACE with a message; nothing is launched. The call
+ * itself performs no cudaMalloc/cudaFree or other allocation.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the one array, and each call overwrites what the
+ * previous one left there: calls that can overlap on the GPU (on different
+ * streams without ordering between them) race on it and must not be issued.
+ */
+int ds_sparse_mla_decode_noalloc(const void* q, const void* kv_pages, int kv_dtype,
+                                 int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                                 const int32_t* idx, const int32_t* lens, int64_t num_rows,
+                                 int num_heads, int k, float scale, void* out, float* lse,
+                                 int32_t* err_flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

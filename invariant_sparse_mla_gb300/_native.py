@@ -64,13 +64,16 @@ def lib():
         L.ds_sparse_mla_prefill.restype = i32
         L.ds_sparse_mla_prefill.argtypes = [vp, vp, i32, i64, vp, i64, i64, vp, vp, vp, i64, i32,
                                             i32, f32, vp, vp, vp, sz, vp, vp]
+        L.ds_sparse_mla_decode_noalloc.restype = i32
+        L.ds_sparse_mla_decode_noalloc.argtypes = [vp, vp, i32, i64, vp, i64, vp, vp, i64, i32,
+                                                   i32, f32, vp, vp, vp, vp]
         _lib = L
         return _lib
 
 
 EXPORTED = ("ds_last_error", "ds_supported_config", "ds_topk_workspace_size",
             "ds_sparse_mla_workspace_size", "ds_topk_per_row", "ds_sparse_mla_decode",
-            "ds_sparse_mla_prefill")
+            "ds_sparse_mla_prefill", "ds_sparse_mla_decode_noalloc")
 
 
 def last_error():

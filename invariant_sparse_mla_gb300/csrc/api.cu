@@ -129,6 +129,20 @@ int attention_common(const char* fn, const void* q, const void* kv_pages, int kv
 
 }  // namespace
 
+namespace dsmla {
+
+int report_error(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+}  // namespace dsmla
+
 extern "C" {
 
 const char* ds_last_error(void) { return g_last_error.c_str(); }

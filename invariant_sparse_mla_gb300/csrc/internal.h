@@ -51,4 +51,8 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
 
 cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream);
 
+// Records a printf-style message for ds_last_error() on this host thread and
+// returns `status`.
+int report_error(int status, const char* fmt, ...);
+
 }  // namespace dsmla
