@@ -78,6 +78,9 @@ int attention_common(const char* fn, const void* q, const void* kv_pages, int kv
     return fail(DS_ERR_UNSUPPORTED, "%s: num_rows=%lld is too large for one launch (max %lld)", fn,
                 (long long)num_rows, (long long)((int64_t)INT32_MAX / (splits * groups * 2)));
   if (num_pages < 1) return fail(DS_ERR_SHAPE, "%s: num_pages=%lld must be >= 1", fn, (long long)num_pages);
+  if (num_pages > (int64_t)INT32_MAX / DS_PAGE_BLOCK_SIZE)
+    return fail(DS_ERR_UNSUPPORTED, "%s: num_pages=%lld exceeds %lld (KV rows are indexed in 32 bits)",
+                fn, (long long)num_pages, (long long)(INT32_MAX / DS_PAGE_BLOCK_SIZE));
   if (bt_stride < 1) return fail(DS_ERR_SHAPE, "%s: bt_stride=%lld must be >= 1", fn, (long long)bt_stride);
   if (num_bt_rows < 1)
     return fail(DS_ERR_SHAPE, "%s: num_requests=%lld must be >= 1", fn, (long long)num_bt_rows);

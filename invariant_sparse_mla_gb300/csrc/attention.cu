@@ -16,9 +16,11 @@
 //   producer warps 4-7  gather 64-entry tiles of 1152-byte bf16 rows into a
 //                       128-byte-swizzled shared-memory tile (FP8 rows are
 //                       dequantised to bf16 on the way), double buffered;
-//   MMA warp 8          one thread issues tcgen05 MMAs:
-//                         S   = Q K^T      M=128 (heads), N=64, K=576 -> TMEM
-//                         O^T += V^T P^T   M=128 (dv block), N=heads, K=64
+//   MMA warps 8, 9      one thread each issues tcgen05 MMAs (two issuers keep
+//                       the tensor pipe fed; a single thread can issue one
+//                       MMA per ~54 cycles):
+//                         warp 8: S = Q K^T      M=64 (heads), N=64, K=576
+//                         warp 9: O^T += V^T P^T M=128 (dv block), N=heads, K=64
 //                       The same swizzled tile is the K-major B operand of
 //                       the first and the MN-major A operand of the second.
 //   softmax warps 0-3   read S from TMEM (one head per TMEM lane), keep a
@@ -27,10 +29,10 @@
 //                       head's max grows by more than 2^8 (exact: p <= 256
 //                       is kept relative to the stored max).
 //
-// Rows of the QK MMA beyond the head group are never read: the A descriptor
-// simply continues into the next swizzle atoms, and a D row depends only on
-// its own A row. Every wait is bounded; a timeout sets DS_DEVERR_TIMEOUT and
-// the CTA winds down, frees its TMEM and exits.
+// The QK MMA has M = 64: for head groups smaller than 64, the A descriptor
+// simply continues into the following smem, and those D rows are never read
+// (a D row depends only on its own A row). Every wait is bounded; a timeout
+// sets DS_DEVERR_TIMEOUT and the CTA winds down, frees its TMEM and exits.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,11 +54,11 @@ constexpr int kDv = 512;
 constexpr int kRowBytesBf16 = kD * 2;                 // 1152
 constexpr int kRowBytesFp8 = 656;
 constexpr int kChunks = kRowBytesBf16 / 16;           // 72 16-byte chunks per bf16 row
-constexpr int kTile = kTileEntries;                   // 32 entries per tile
-constexpr int kStages = 4;                            // KV tile ring
-constexpr int kStageBytes = kTile * kRowBytesBf16;    // 36864
+constexpr int kTile = kTileEntries;                   // 64 entries per tile
+constexpr int kStages = 2;                            // KV tile ring
+constexpr int kStageBytes = kTile * kRowBytesBf16;    // 73728
 constexpr int kAtomStride = kTile * 128;              // bytes between 64-dim column blocks
-constexpr int kThreads = 288;                         // 9 warps
+constexpr int kThreads = 320;                         // 10 warps
 constexpr int kSCols = kTile;                         // TMEM columns of one S buffer
 constexpr int kOCol = 2 * kSCols;                     // first TMEM column of O^T
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
@@ -69,11 +71,11 @@ struct Layout {
   static constexpr int kQBytes = HG * kRowBytesBf16;
   static constexpr int kQ = 0;
   static constexpr int kKV = kQ + kQBytes;                    // kStages x kStageBytes
-  static constexpr int kP = kKV + kStages * kStageBytes;      // HG rows x 128 B: two P tiles
+  static constexpr int kP = kKV + kStages * kStageBytes;      // HG rows x 128 B (64 entries)
   static constexpr int kPBytes = HG * 128;
-  static constexpr int kBars = kP + kPBytes;                  // 24 x u64
-  static constexpr int kMask = kBars + 24 * 8;                // kSplitTiles x u32
-  static constexpr int kAlpha = kMask + kSplitTiles * 4;      // 2 x 64 floats
+  static constexpr int kBars = kP + kPBytes;                  // 16 x u64
+  static constexpr int kMask = kBars + 16 * 8;                // kSplitTiles x u64
+  static constexpr int kAlpha = kMask + kSplitTiles * 8;      // 2 x 64 floats
   static constexpr int kTmemSlot = kAlpha + 2 * 64 * 4;       // u32
   static constexpr int kNeff = kTmemSlot + 4;                 // int
   static constexpr int kEnd = kNeff + 12;
@@ -81,18 +83,18 @@ struct Layout {
   static constexpr uint32_t kTmemCols = (kOCol + 4 * HG) <= 256 ? 256u : 512u;
 };
 
-// Barrier slots. Every barrier that is waited on by parity is only ever
-// waited on for a phase that cannot be overtaken by the next one (each has
-// one in-flight use at a time), so the parity test is unambiguous.
+// Barrier slots. Every barrier waited on by parity is only ever waited on
+// for a phase that cannot be overtaken by the next one, so the parity test
+// is unambiguous.
 enum Bar {
-  kQFull = 0,
-  kKvFull = 1,     // 4: producer threads -> MMA (tile landed)
-  kKvEmpty = 5,    // 4: MMA commit -> producers (stage free)
-  kSFull = 9,      // 2: MMA commit -> softmax (S ready)
-  kPFull = 11,     // 2: softmax threads -> MMA (P written)
-  kPvDone = 13,    // 2: MMA commit -> softmax (PV of a tile done)
-  kMmaDone = 15,
-  kNumBars = 16
+  kQFull = 0,      // loader threads -> QK issuer (Q landed)
+  kKvFull = 1,     // 2: loader threads -> QK issuer (tile landed)
+  kKvEmpty = 3,    // 2: PV issuer commit -> loaders (stage free)
+  kSFull = 5,      // 2: QK issuer commit -> softmax (S ready)
+  kPFull = 7,      // 2: softmax threads -> PV issuer, QK issuer (P written, S read)
+  kPvDone = 9,     // PV issuer commit -> softmax (PV of a tile done)
+  kMmaDone = 10,   // 2: each issuer's final drain
+  kNumBars = 12
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -143,6 +145,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+// Starts an asynchronous copy of `bytes` (a multiple of 16, 16-byte aligned
+// source) from global memory into L2, without waiting for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 struct KParams {
   const __nv_bfloat16* q;
   const uint8_t* kv;
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kBars);
-  uint32_t* vmask = reinterpret_cast<uint32_t*>(smem + LY::kMask);
+  uint32_t* vmask = reinterpret_cast<uint32_t*>(smem + LY::kMask);   // 2 words per tile
   float* alpha_s = reinterpret_cast<float*>(smem + LY::kAlpha);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kTmemSlot);
   int* neff_s = reinterpret_cast<int*>(smem + LY::kNeff);
@@ -181,8 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // Warps 4-7 load Q and every KV tile together: warp pw fills rows
+  // 16 pw .. 16 pw + 15 of each tile. For the page lookups, lane l of warp pw
+  // owns row 16 pw + (l & 15) of tiles (l >> 4) + 2i, i = 0..3.
   const bool producer = warp >= 4 && warp < 8;
-  const int pw = warp - 4;          // producer warp 0..3: rows 8*pw .. 8*pw+7 of every tile
+  const int pw = warp - 4;
 
   int64_t bid = blockIdx.x;
   const int hg = (int)(bid % p.num_hg);
@@ -205,86 +216,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
   const int32_t* idx_row = p.idx + row * (int64_t)p.k;
   const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
 
-  // ---- prologue 1: Q copies start; producers read this split's idx entries.
-  // Producer warp pw owns the tiles t = pw + 4i (always stage pw of the ring);
-  // lane l owns row l of each of them.
-  int pos[4] = {-1, -1, -1, -1};
-  if (tid == 0) *neff_s = 0;
-  __syncthreads();
-  if (producer) {
-    const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
-    const int ptid = tid - 128;
-    for (int c = ptid; c < HG * kChunks; c += 128) {
-      const int h = c / kChunks, ch = c - h * kChunks;
-      cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
-    }
-    cp_async_commit();
-    int last = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = pw + 4 * i;
-      if (t < ntiles) {
-        pos[i] = idx_row[j0 + t * kTile + lane];
-        if (pos[i] != -1) last = t + 1;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-    if (lane == 0 && last > 0) atomicMax(neff_s, last);
-  }
-  __syncthreads();
-  const int n_eff = row_ok ? *neff_s : 0;
-
-  if (!row_ok && tid == 0 && p.err != nullptr) atomicOr(p.err, kErrRowReq);
-  if (n_eff == 0) {  // nothing to attend to in this split
-    if (producer) cp_async_wait_all();  // Q copies must land before the CTA exits
-    if (tid < HG) {
-      p.part_m[part_base + tid] = -INFINITY;
-      p.part_l[part_base + tid] = 0.0f;
-    }
-    return;
-  }
-
-  // ---- prologue 2: page lookups and validity masks; barriers; TMEM.
-  int64_t grow[4] = {-1, -1, -1, -1};   // global KV row of each owned entry, -1 = skip
-  if (producer) {
-    int err_bits = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = pw + 4 * i;
-      bool valid = false;
-      if (t < n_eff) {
-        const int ps = pos[i];
-        if (ps >= 0 && (int64_t)ps < len) {
-          const int64_t blk = ps >> 6;
-          if (blk < p.bt_stride) {
-            const int64_t page = p.block_table[bt_row * p.bt_stride + blk];
-            if (page >= 0 && page < p.num_pages) {
-              grow[i] = page * 64 + (ps & 63);
-              valid = true;
-            } else {
-              err_bits |= kErrPage;
-            }
-          } else {
-            err_bits |= kErrPage;
-          }
-        } else if (ps != -1) {
-          err_bits |= kErrIdx;
-        }
-      }
-      const uint32_t ballot = __ballot_sync(0xffffffffu, valid);
-      if (lane == 0 && t < kSplitTiles) vmask[t] = ballot;
-    }
-    if (err_bits && p.err != nullptr) atomicOr(p.err, err_bits);
-  }
+  // ---- prologue (one block-wide barrier): producers start the Q copies,
+  // read their idx entries and resolve pages; thread 0 sets up the
+  // barriers; warp 8 allocates TMEM.
   if (tid == 0) {
+    *neff_s = 0;
     for (int i = 0; i < kNumBars; ++i) {
-      // q_full and p_full take one arrival per producer / softmax thread,
-      // kv_full one per lane of the warp that owns the stage, the rest one
-      // tcgen05.commit.
+      // q_full, kv_full and p_full: one arrival per loader / softmax
+      // thread; the rest: one tcgen05.commit.
       uint32_t count = 1u;
       if (i == kQFull || i == kPFull || i == kPFull + 1) count = 128u;
-      if (i >= kKvFull && i < kKvFull + kStages) count = 32u;
+      if (i >= kKvFull && i < kKvFull + kStages) count = 128u;
       mbar_init(&bars[i], count);
     }
     mbar_fence_init();
@@ -293,55 +235,133 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
     tmem_alloc(tmem_slot, LY::kTmemCols);
     tmem_relinquish();
   }
+  __syncthreads();   // neff_s = 0 is visible before any atomicMax below
+  // KV row (page * 64 + slot) of each owned entry, -1 = skip: slot i is
+  // tile (lane >> 4) + 2i, row 16 pw + (lane & 15).
+  int grow[4] = {-1, -1, -1, -1};
+  if (producer) {
+    const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
+    const int ptid = tid - 128;
+    for (int c = ptid; c < HG * kChunks; c += 128) {
+      const int h = c / kChunks, ch = c - h * kChunks;
+      cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
+    }
+    cp_async_commit();
+    int pos[4];
+    int last = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = (lane >> 4) + 2 * i;
+      pos[i] = t < ntiles ? idx_row[j0 + t * kTile + pw * 16 + (lane & 15)] : -1;
+      if (pos[i] != -1) last = t + 1;
+    }
+    int err_bits = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ps = pos[i];
+      bool valid = false;
+      if (ps >= 0 && (int64_t)ps < len && row_ok) {
+        const int64_t blk = ps >> 6;
+        if (blk < p.bt_stride) {
+          const int64_t page = p.block_table[bt_row * p.bt_stride + blk];
+          if (page >= 0 && page < p.num_pages) {
+            grow[i] = (int)(page * 64 + (ps & 63));
+            valid = true;
+          } else {
+            err_bits |= kErrPage;
+          }
+        } else {
+          err_bits |= kErrPage;
+        }
+      } else if (ps != -1 && row_ok) {
+        err_bits |= kErrIdx;
+      }
+      const uint32_t ballot = __ballot_sync(0xffffffffu, valid);
+      if (lane == 0) {
+        // lanes 0-15: tile 2i, lanes 16-31: tile 2i + 1; 16 rows per warp.
+        reinterpret_cast<uint16_t*>(vmask + 2 * (2 * i))[pw] = (uint16_t)(ballot & 0xFFFFu);
+        reinterpret_cast<uint16_t*>(vmask + 2 * (2 * i + 1))[pw] = (uint16_t)(ballot >> 16);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    if (lane == 0 && last > 0) atomicMax(neff_s, last);
+    if (err_bits && p.err != nullptr) atomicOr(p.err, err_bits);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int n_eff = row_ok ? *neff_s : 0;
+  if (!row_ok && tid == 0 && p.err != nullptr) atomicOr(p.err, kErrRowReq);
 
   bool failed = false;
-
-  if (producer) {
+  if (n_eff == 0) {
+    // Nothing to attend to in this split: an empty partial.
+    if (producer) cp_async_wait_all();  // Q copies must land before the CTA exits
+    if (tid < HG) {
+      p.part_m[part_base + tid] = -INFINITY;
+      p.part_l[part_base + tid] = 0.0f;
+    }
+  } else if (producer) {
     // ------------------------------------------------------------ producers
-    // Warp pw fills stage pw with tiles pw, pw+4, ...: it waits for its own
-    // copies (or stores) to land, fences them for the tensor core and
-    // arrives; the four warps keep four tiles in flight.
-    const uint32_t stage_base = sbase + LY::kKV + pw * kStageBytes;
-    bool q_signalled = false;
+    // All four warps fill each tile in turn (16 rows each) into stage t & 1,
+    // wait for their own copies (or stores) to land, fence them for the
+    // tensor core and arrive. Q shares the first tile's wait. Right after
+    // tile 0 is under way, every other selected row of the split is streamed
+    // into L2: shared memory holds only two tiles, the L2 (129 MB) holds all
+    // of them, so the HBM reads of later tiles overlap the compute of earlier
+    // ones and their smem copies hit L2.
 #pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-      const int t = pw + 4 * i;
-      if (t >= n_eff) break;
-      const int64_t gi = i == 0 ? grow[0] : i == 1 ? grow[1] : i == 2 ? grow[2] : grow[3];
-      const bool ok = i == 0 || mbar_wait(&bars[kKvEmpty + pw], (i - 1) & 1);
+    for (int t = 0; t < n_eff; ++t) {
+      const int stage = t & 1;
+      const uint32_t stage_base = sbase + LY::kKV + stage * kStageBytes;
+      const bool ok = t < 2 || mbar_wait(&bars[kKvEmpty + stage], ((t >> 1) - 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         failed = true;
         break;
       }
+      const int sel = t >> 1;
+      const int gi = sel == 0 ? grow[0] : sel == 1 ? grow[1] : sel == 2 ? grow[2] : grow[3];
+      const int src_lane0 = (t & 1) << 4;
       if constexpr (!FP8) {
 #pragma unroll 4
-        for (int rr = 0; rr < kTile; ++rr) {
-          const int64_t g = __shfl_sync(0xffffffffu, gi, rr);
+        for (int rr = 0; rr < 16; ++rr) {
+          const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + rr);
           const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             const int c = lane + 32 * j;
             if (c < kChunks)
-              cp_async_16(stage_base + swz_off(rr, c, kAtomStride), src + c * 16, nbytes);
+              cp_async_16(stage_base + swz_off(pw * 16 + rr, c, kAtomStride), src + c * 16,
+                          nbytes);
           }
         }
         cp_async_commit();
+        if (t == 0) {
+#pragma unroll
+          for (int i = 1; i < 4; ++i)
+            if (grow[i] >= 0)
+              prefetch_l2_bulk(p.kv + (int64_t)grow[i] * kRowBytesBf16, (uint32_t)kRowBytesBf16);
+        }
         cp_async_wait_all();
       } else {
-        if (i == 0) cp_async_wait_all();   // Q
+        if (t == 0) {
+#pragma unroll
+          for (int i = 1; i < 4; ++i)
+            if (grow[i] >= 0)
+              prefetch_l2_bulk(p.kv + (int64_t)grow[i] * kRowBytesFp8, (uint32_t)kRowBytesFp8);
+          cp_async_wait_all();   // Q
+        }
 #pragma unroll 1
-        for (int r0 = 0; r0 < kTile; r0 += 8) {
+        for (int r0 = 0; r0 < 16; r0 += 8) {
           uint2 codes[8][2];
           float scl[8][2];
           uint4 rope[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const int64_t g = __shfl_sync(0xffffffffu, gi, r0 + u);
+            const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + r0 + u);
             const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesFp8;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -354,11 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
               }
             }
             rope[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (lane < 8 && g >= 0) rope[u] = *reinterpret_cast<const uint4*>(src + 528 + lane * 16);
+            if (lane < 8 && g >= 0)
+              rope[u] = *reinterpret_cast<const uint4*>(src + 528 + lane * 16);
           }
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const int tr = r0 + u;
+            const int tr = pw * 16 + r0 + u;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int c = lane + 32 * j;
@@ -370,109 +391,107 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
         }
       }
       fence_proxy_async_smem();
-      if (!q_signalled) {
-        mbar_arrive(&bars[kQFull]);
-        q_signalled = true;
-      }
-      mbar_arrive(&bars[kKvFull + pw]);
-    }
-    if (!q_signalled && !failed) {   // this warp had no tile: still release Q
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      mbar_arrive(&bars[kQFull]);
+      if (t == 0) mbar_arrive(&bars[kQFull]);
+      mbar_arrive(&bars[kKvFull + stage]);
     }
     cp_async_wait_all();
   } else if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK issuer
+    // QK(t) needs tile t landed and its S buffer free: P(t-2) written means
+    // softmax(t-2) has read S(t-2). Descriptors are precomputed; the 36 MMAs
+    // of a tile are issued back to back.
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_bf16(128, kTile, 0, 0);
-      constexpr uint32_t idesc_pv = make_idesc_bf16(128, HG, 1, 0);
-      const uint32_t q_addr = sbase + LY::kQ;
-      const uint32_t p_addr = sbase + LY::kP;
-      auto issue_pv = [&](int t) {
-        const uint32_t kv_addr = sbase + LY::kKV + (t & (kStages - 1)) * kStageBytes;
-        const uint32_t p_tile = p_addr + (t & 1) * (kTile * 2);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t a = make_sw128_desc(kv_addr + 2 * b * kAtomStride + kk * 2048,
-                                               kAtomStride, 1024);
-            const uint64_t bd = make_sw128_desc(p_tile + kk * 32, 16, 1024);
-            mma_bf16_ss(tmem + kOCol + b * HG, a, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-      };
+      constexpr uint32_t idesc_qk = make_idesc_bf16(64, kTile, 0, 0);
+      const uint64_t q_desc = make_sw128_desc(sbase + LY::kQ, 16, 1024);
+      const uint64_t kv_desc0 = make_sw128_desc(sbase + LY::kKV, 16, 1024);
       if (!mbar_wait(&bars[kQFull], 0)) failed = true;
       for (int t = 0; t < n_eff && !failed; ++t) {
-        const int stage = t & (kStages - 1);
-        if (!mbar_wait(&bars[kKvFull + stage], (t / kStages) & 1)) {
+        const int sb = t & 1;
+        if (!mbar_wait(&bars[kKvFull + sb], (t >> 1) & 1) ||
+            (t >= 2 && !mbar_wait(&bars[kPFull + sb], ((t >> 1) - 1) & 1))) {
           failed = true;
           break;
         }
         tc_fence_after();
-        const uint32_t kv_addr = sbase + LY::kKV + stage * kStageBytes;
-#pragma unroll 4
+        const uint64_t b0 = kv_desc0 + (uint64_t)((sb * kStageBytes) >> 4);
+        const uint32_t d = tmem + sb * kSCols;
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const int ka = kk >> 2;
-          const uint32_t off = (kk & 3) * 32;
-          const uint64_t a = make_sw128_desc(q_addr + ka * (HG * 128) + off, 16, 1024);
-          const uint64_t b = make_sw128_desc(kv_addr + ka * kAtomStride + off, 16, 1024);
-          mma_bf16_ss(tmem + (t & 1) * kSCols, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t ka = kk >> 2, off = (kk & 3) * 32;
+          mma_bf16_ss(d, q_desc + ((ka * (HG * 128) + off) >> 4),
+                      b0 + ((ka * kAtomStride + off) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars[kSFull + (t & 1)]);
-        if (t >= 1) {
-          const int u = t - 1;
-          if (!mbar_wait(&bars[kPFull + (u & 1)], (u >> 1) & 1)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(u);
-          mma_commit(&bars[kKvEmpty + (u & (kStages - 1))]);
-          mma_commit(&bars[kPvDone + (u & 1)]);
-        }
+        mma_commit(&bars[kSFull + sb]);
       }
-      if (!failed) {
-        const int u = n_eff - 1;
-        if (mbar_wait(&bars[kPFull + (u & 1)], (u >> 1) & 1)) {
-          tc_fence_after();
-          issue_pv(u);
-          mma_commit(&bars[kPvDone + (u & 1)]);
-        } else {
-          failed = true;
-        }
-      }
-      // Drain: wait until every MMA issued above has completed.
       mma_commit(&bars[kMmaDone]);
       mbar_wait(&bars[kMmaDone], 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ PV issuer
+    // PV(t) needs P(t); its completion frees the KV stage and lets softmax
+    // overwrite P and rescale O^T.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, HG, 1, 0);
+      const uint64_t p_desc = make_sw128_desc(sbase + LY::kP, 16, 1024);
+      const uint64_t v_desc0 = make_sw128_desc(sbase + LY::kKV, kAtomStride, 1024);
+      for (int t = 0; t < n_eff && !failed; ++t) {
+        const int sb = t & 1;
+        if (!mbar_wait(&bars[kPFull + sb], (t >> 1) & 1)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t a0 = v_desc0 + (uint64_t)((sb * kStageBytes) >> 4);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            mma_bf16_ss(tmem + kOCol + b * HG, a0 + (((2 * b * kAtomStride) + kk * 2048) >> 4),
+                        p_desc + ((kk * 32) >> 4), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&bars[kKvEmpty + sb]);
+        mma_commit(&bars[kPvDone]);
+      }
+      mma_commit(&bars[kMmaDone + 1]);
+      mbar_wait(&bars[kMmaDone + 1], 0);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
     // ------------------------------------------------------------ softmax
-    const int h = tid;               // TMEM lane == S row == head in group
-    const bool warp_has_heads = warp * 32 < HG;
+    // S was computed with M = 64: head h sits in TMEM lane 32*(h/16) + h%16,
+    // so every softmax warp holds 16 heads (its lanes 0-15). With the
+    // 16x32bx2 load, lane l and lane l+16 both read head 16*warp + l%16:
+    // entries 0-31 and 32-63 of the tile respectively. Row max and sum are
+    // combined between the two with one shuffle.
+    const int hl = lane & 15;
+    const int half = lane >> 4;
+    const int h = warp * 16 + hl;
+    const bool active = h < HG;
+    const bool warp_has_heads = warp * 16 < HG;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     uint8_t* prow = smem + LY::kP + (h >> 3) * 1024 + (h & 7) * 128;
-    float m = -INFINITY, l = 0.0f;
-    float s[kSCols];
-    // All four softmax warps meet at named barriers (ids 1-3), so every
+    float m = -INFINITY, l = 0.0f;   // l: this half's share of the row sum
+    float s[32];
+    // The four softmax warps meet at named barriers (ids 1-2), so every
     // timeout decision is made jointly: either all leave the loop or none.
     for (int t = 0; t < n_eff; ++t) {
       const int sb = t & 1;
-      const bool ok = mbar_wait(&bars[kSFull + sb], (t >> 1) & 1);
+      bool ok = mbar_wait(&bars[kSFull + sb], (t >> 1) & 1);
       bool need = false;
       if (ok) {
         tc_fence_after();
         if (warp_has_heads) {
-          tmem_ld32_sync(tmem + lane_base + sb * kSCols, s);
-          const uint32_t mask = vmask[t];
+          tmem_ld16x32bx2_x32_sync(tmem + lane_base + sb * kSCols, s);
+          const uint32_t mask = vmask[2 * t + half];
           float mt = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < kSCols; ++j) {
+          for (int j = 0; j < 32; ++j) {
             s[j] = ((mask >> j) & 1u) ? s[j] * p.scale_log2 : -INFINITY;
             mt = fmaxf(mt, s[j]);
           }
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
           float a = 1.0f;
           if (mt > m + kRescaleThreshold) {
             a = (m == -INFINITY) ? 0.0f : ex2(m - mt);
@@ -480,43 +499,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
             l *= a;
             m = mt;
           }
-          if (h < HG) alpha_s[sb * 64 + h] = a;
+          if (active && half == 0) alpha_s[sb * 64 + h] = a;
         }
+        // P(t) overwrites P(t-1) and O^T may be rescaled: PV(t-1) must be done.
+        if (t > 0) ok = mbar_wait(&bars[kPvDone], (t - 1) & 1);
       }
       if (named_bar_or(1, 128, !ok)) {
         failed = true;
         break;
       }
-      const bool any = named_bar_or(2, 128, need);
-      // Rescaling O^T needs PV(t-1) complete; reusing P buffer t&1 needs PV(t-2).
-      bool ok2 = true;
-      if (any) ok2 = mbar_wait(&bars[kPvDone + ((t - 1) & 1)], ((t - 1) >> 1) & 1);
-      else if (t >= 2) ok2 = mbar_wait(&bars[kPvDone + (t & 1)], ((t >> 1) - 1) & 1);
-      if (named_bar_or(3, 128, !ok2)) {
-        failed = true;
-        break;
-      }
+      const bool any = named_bar_or(2, 128, need && active);
       tc_fence_after();
-      if (any) {
-        // O^T lanes are dv rows; columns are heads. Scale column h by alpha[h].
-#pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
-#pragma unroll
-          for (int c = 0; c < HG / 16; ++c) {
-            float v[16];
-            const uint32_t addr = tmem + lane_base + kOCol + b * HG + 16 * c;
-            tmem_ld16_sync(addr, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] *= alpha_s[sb * 64 + 16 * c + i];
-            tmem_st16(addr, v);
-          }
-        }
-        tmem_wait_st();
-      }
-      if (warp_has_heads && h < HG) {
+      if (active) {
         float lsum = 0.0f;
 #pragma unroll
-        for (int c4 = 0; c4 < kTile / 8; ++c4) {
+        for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -528,17 +525,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
             lsum += pr.y;
             w[i] = *reinterpret_cast<const uint32_t*>(&pb);
           }
-          const int c = sb * (kTile / 8) + c4;   // 16-byte chunk within the 128-byte row
-          st_shared_v4(smem_u32(prow) + ((c ^ (h & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+          const int c8 = 4 * half + c4;   // 16-byte chunk of the 128-byte P row
+          st_shared_v4(smem_u32(prow) + ((c8 ^ (h & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
         }
         l += lsum;
+      }
+      if (any) {
+        // O^T lanes are dv rows; columns are heads. Scale column h by alpha[h].
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+#pragma unroll 1
+          for (int c = 0; c < HG / 16; ++c) {
+            float v[16];
+            const uint32_t addr = tmem + lane_base + kOCol + b * HG + 16 * c;
+            tmem_ld16_sync(addr, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= alpha_s[sb * 64 + 16 * c + i];
+            tmem_st16(addr, v);
+          }
+        }
+        tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[kPFull + sb]);
     }
-    const int u = n_eff - 1;
-    if (!failed && !mbar_wait(&bars[kPvDone + (u & 1)], (u >> 1) & 1)) failed = true;
+    if (!failed && !mbar_wait(&bars[kPvDone], (n_eff - 1) & 1)) failed = true;
     if (!failed) {
       tc_fence_after();
       // Epilogue: partial O (unnormalised, relative to m), m and l.
@@ -546,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       float* po = p.part_o + part_base * kDv;
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < HG / 16; ++c) {
           float v[16];
           tmem_ld16_sync(tmem + lane_base + kOCol + b * HG + 16 * c, v);
@@ -554,9 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
           for (int i = 0; i < 16; ++i) po[(int64_t)(16 * c + i) * kDv + 128 * b + dv_lane] = v[i];
         }
       }
-      if (h < HG) {
+      const float l_other = __shfl_xor_sync(0xffffffffu, l, 16);
+      if (active && half == 0) {
         p.part_m[part_base + h] = m;
-        p.part_l[part_base + h] = l;
+        p.part_l[part_base + h] = l + l_other;
       }
     }
   }

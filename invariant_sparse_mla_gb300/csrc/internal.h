@@ -9,8 +9,8 @@ namespace dsmla {
 // Entries per attention tile and tiles per split. The split count of a call
 // is ceil(k / kSplitEntries): a function of k alone, so a row's reduction
 // order never depends on the batch.
-constexpr int kTileEntries = 32;
-constexpr int kSplitTiles = 16;
+constexpr int kTileEntries = 64;
+constexpr int kSplitTiles = 8;
 constexpr int kSplitEntries = kTileEntries * kSplitTiles;
 
 inline int num_splits_for_k(int k) { return (k + kSplitEntries - 1) / kSplitEntries; }
