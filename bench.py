@@ -40,9 +40,17 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 WORKLOAD = "tp2_decode"
-WORKLOAD_DESC = ("TP2-shaped sparse MLA decode: batch 32, 64 heads, contexts uniform int in "
-                 "[4096, 32768], topk 2048, bf16 paged latent KV (page 64, random block-table "
-                 "permutation), d_qk 576 (512+64), d_v 512, fp32 N(0,1) scores, scale 1/sqrt(576)")
+WORKLOAD_DESCS = {
+    "tp2_decode": ("TP2-shaped sparse MLA decode: batch 32, 64 heads, contexts uniform int in "
+                   "[4096, 32768], topk 2048, bf16 paged latent KV (page 64, random block-table "
+                   "permutation), d_qk 576 (512+64), d_v 512, fp32 N(0,1) scores, scale 1/sqrt(576)"),
+    "tp1_fp8_decode": ("TP1 sparse MLA decode at scale: batch 128, 128 heads, contexts uniform int in "
+                       "[8192, 131072], topk 2048, FP8 e4m3 latent KV (fp32 scale per 128 dims) + "
+                       "bf16 rope, page 64, fp32 N(0,1) scores"),
+    "chunked_prefill": ("chunked sparse MLA prefill: 1 request, 4096 query tokens at positions "
+                        "61440..65535 of a 65536 context, causal, topk 2048, 128 heads, bf16 KV, "
+                        "fp32 N(0,1) scores"),
+}
 METRIC = "sparse-MLA decode tokens/s and top-k rows/s on 1 GB300; % of roofline"
 N_SETS = 4
 HBM_CONTRACT_GBS = 8000.0
@@ -58,6 +66,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sets", type=int, default=N_SETS,
                     help="rotating input sets (profiling runs use 1 to stay small)")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESCS), default=WORKLOAD,
+                    help="the TP2 decode batch is the headline; the others are for the record")
     return ap.parse_args()
 
 
@@ -199,15 +209,21 @@ def algorithmic_bytes(case, idx):
     """Bytes the path must move at minimum (no re-reads, no workspaces).
 
     top-k: every in-range score read once (4 B) + idx written (4 B each).
-    attention: every valid selected KV row read once (1152 B bf16) + q read
-    + out (bf16) and lse written + idx read.
+    attention: every distinct selected KV row read once (1152 B bf16 or
+    656 B FP8; prefill tokens of one request share rows) + q read + out
+    (bf16) and lse written + idx read. FLOPs: 2 * H * (576 + 512) per valid
+    selected entry.
     """
     import torch
     L = (case.row_ends - case.row_starts).clamp(min=0).to(torch.int64)
     topk = 4 * int(L.sum()) + 4 * idx.numel()
-    valid = int((idx >= 0).sum())
+    valid_mask = idx >= 0
+    valid = int(valid_mask.sum())
+    key = case.row_req.to(torch.int64)[:, None] * (1 << 32) + idx.to(torch.int64)
+    distinct = int(torch.unique(key[valid_mask]).numel())
+    row_bytes = 1152 if case.kv_dtype == "bf16" else 656
     R, H = case.q.shape[0], case.q.shape[1]
-    attn = valid * 1152 + case.q.numel() * 2 + R * H * 512 * 2 + R * H * 4 + idx.numel() * 4
+    attn = distinct * row_bytes + case.q.numel() * 2 + R * H * 512 * 2 + R * H * 4 + idx.numel() * 4
     flops = 2 * valid * H * (576 + 512)
     return topk, attn, flops
 
@@ -221,16 +237,20 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     sets = []
     n_sets = args.sets
+    from synthetic import WORKLOADS, decode_case, prefill_case, _uniform_ints
+    wl = args.workload
+    w = WORKLOADS[wl]
     for s in range(n_sets):
-        c = workload_case(WORKLOAD, device="cuda")
-        if s > 0 or rank > 0:
-            # Independent batches: reseed by regenerating with a shifted seed.
-            from synthetic import WORKLOADS, decode_case, _uniform_ints
-            w = WORKLOADS[WORKLOAD]
-            seed = w["seed"] + 1000 * rank + 17 * s
-            ctx = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], seed)
-            c = decode_case(WORKLOAD, ctx, w["H"], w["k"], w["kv"], seed, w["scores"],
-                            stride=w["stride"], device="cuda")
+        # Independent batches per set and rank: the same recipe, shifted seeds.
+        seed = w["seed"] + 1000 * rank + 17 * s
+        if w["kind"] == "decode":
+            ctx = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if s == 0 and rank == 0
+                                else seed)
+            c = decode_case(wl, ctx, w["H"], w["k"], w["kv"], seed if s or rank else w["seed"],
+                            w["scores"], stride=w["stride"], device="cuda")
+        else:
+            c = prefill_case(wl, w["ctx"], w["first_pos"], w["T"], w["H"], w["k"], w["kv"],
+                             seed if s or rank else w["seed"], device="cuda")
         R, H, k = c.q.shape[0], c.H, c.k
         c.idx = torch.empty((R, k), dtype=torch.int32, device=dev)
         c.out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
@@ -244,8 +264,13 @@ def run_ours(args, rank, world, local):
         ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k, idx_out=c.idx, stream=stream)
 
     def decode(c):
-        ds.sparse_mla_decode(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.idx, c.lens, c.scale,
-                             out=c.out, lse=c.lse, workspace=c.ws, stream=stream)
+        if w["kind"] == "decode":
+            ds.sparse_mla_decode(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.idx, c.lens,
+                                 c.scale, out=c.out, lse=c.lse, workspace=c.ws, stream=stream)
+        else:
+            ds.sparse_mla_prefill(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.row_req, c.idx,
+                                  c.lens, c.scale, out=c.out, lse=c.lse, workspace=c.ws,
+                                  stream=stream)
 
     def step(c):
         topk(c)
@@ -309,7 +334,7 @@ def run_ours(args, rank, world, local):
     topk_bytes, attn_bytes, attn_flops = (sum(tb) / n_sets, sum(ab) / n_sets, sum(fl) / n_sets)
 
     # End to end through the public API with pinned host buffers.
-    e2e = None if args.no_e2e else run_e2e(ds, sets, stream, dev,
+    e2e = None if (args.no_e2e or w["kind"] != "decode") else run_e2e(ds, sets, stream, dev,
                                            steps_e2e=max(20, min(400, args.steps // 50)),
                                            world=world)
 
@@ -320,9 +345,19 @@ def run_ours(args, rank, world, local):
     attn_gbs = attn_bytes / dec_s / 1e9
     topk_gbs = topk_bytes / topk_s / 1e9
     roof_s = max(attn_bytes / (HBM_CONTRACT_GBS * 1e9), attn_flops / (tflops * 1e12))
+    tensor_bound = attn_flops / (tflops * 1e12) > attn_bytes / (hbm * 1e9)
+    attn_tflops = attn_flops / dec_s / 1e12
+    if tensor_bound:
+        roof = {"bound": "tensor", "kernel": "sparse_mla attention (split + combine)",
+                "achieved": round(attn_tflops, 1), "peak": tflops, "unit": "TFLOP/s",
+                "frac": round(attn_tflops / tflops, 4), "peak_kind": f"{peak_kind} bf16 dense",
+                "traffic": None, "algorithmic_flops": round(attn_flops),
+                "frac_of_contract_roofline": round(roof_s / dec_s, 4)}
+    else:
+        roof = None
     traffic = ncu_traffic()
     line = {
-        "metric": METRIC,
+        "metric": METRIC if wl == WORKLOAD else METRIC + f" [{wl}]",
         "value": round(value, 1),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -332,9 +367,9 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if sets[0].kv_dtype == "bf16" else "bf16 (FP8 e4m3 KV dequantised to bf16)",
         "data": "synthetic (seeded; random-init latent KV, N(0,1) scores)",
-        "config": {"workload": WORKLOAD_DESC, "global_batch": R * world, "heads": H, "topk": k,
+        "config": {"workload": WORKLOAD_DESCS[wl], "global_batch": R * world, "heads": H, "topk": k,
                    "parallelism": f"replicas x{world} (rows independent, no collective)",
                    "l2": f"{n_sets} rotating input sets, {n_sets * attn_bytes / 1e6:.0f} MB of "
                          f"gathered KV vs 129 MB L2", "cuda_graph": True},
@@ -352,10 +387,15 @@ def run_ours(args, rank, world, local):
                           "unit": "GB/s", "frac": round(topk_gbs / hbm, 4),
                           "algorithmic_bytes": round(topk_bytes)},
         "e2e": e2e,
+        "attention_tflops": round(attn_tflops, 1),
         "gpu_launches": launches,
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_cpu_baseline and world == 1:
+    if roof is not None:
+        line["roofline"] = roof
+    if wl != WORKLOAD or traffic is None:
+        line["roofline"]["traffic"] = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1 and wl == WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(sets[0], budget_s=10.0)
     return line
 
@@ -489,7 +529,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": n, "steps_requested": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t_used / max(n, 1) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": WORKLOAD_DESC, "global_batch": R,
+            "config": {"workload": WORKLOAD_DESCS[WORKLOAD], "global_batch": R,
                        "parallelism": "CPU oracle, rank 0"},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
                              "kind": "oracle", "sample": sample},

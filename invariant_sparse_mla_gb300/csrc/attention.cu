@@ -16,11 +16,13 @@
 //   producer warps 4-7  gather 64-entry tiles of 1152-byte bf16 rows into a
 //                       128-byte-swizzled shared-memory tile (FP8 rows are
 //                       dequantised to bf16 on the way), double buffered;
-//   MMA warps 8, 9      one thread each issues tcgen05 MMAs (two issuers keep
-//                       the tensor pipe fed; a single thread can issue one
-//                       MMA per ~54 cycles):
-//                         warp 8: S = Q K^T      M=64 (heads), N=64, K=576
-//                         warp 9: O^T += V^T P^T M=128 (dv block), N=heads, K=64
+//   MMA warps 8-10      one thread each issues tcgen05 MMAs (a single thread
+//                       can issue one MMA per ~54 cycles, so three issuers
+//                       keep the tensor pipe fed):
+//                         warps 8, 10: S = Q K^T M=64 (heads), N=64, over
+//                                      dims 0-319 and 320-575 into two TMEM
+//                                      accumulators summed by the softmax
+//                         warp 9:  O^T += V^T P^T M=128 (dv block), N=heads, K=64
 //                       The same swizzled tile is the K-major B operand of
 //                       the first and the MN-major A operand of the second.
 //   softmax warps 0-3   read S from TMEM (one head per TMEM lane), keep a
@@ -58,9 +60,11 @@ constexpr int kTile = kTileEntries;                   // 64 entries per tile
 constexpr int kStages = 2;                            // KV tile ring
 constexpr int kStageBytes = kTile * kRowBytesBf16;    // 73728
 constexpr int kAtomStride = kTile * 128;              // bytes between 64-dim column blocks
-constexpr int kThreads = 320;                         // 10 warps
+constexpr int kThreads = 352;                         // 11 warps
 constexpr int kSCols = kTile;                         // TMEM columns of one S buffer
-constexpr int kOCol = 2 * kSCols;                     // first TMEM column of O^T
+constexpr int kSbCol = 2 * kSCols;                    // second QK accumulator (2 buffers)
+constexpr int kOCol = 4 * kSCols;                     // first TMEM column of O^T
+constexpr int kQkSplitAtom = 5;                       // QK column blocks [0,5) -> S_a, [5,9) -> S_b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 
 // Error bits (match DS_DEVERR_* in the public header).
@@ -80,21 +84,21 @@ struct Layout {
   static constexpr int kNeff = kTmemSlot + 4;                 // int
   static constexpr int kEnd = kNeff + 12;
   static constexpr int kSmemBytes = kEnd + 1024;              // + alignment slack
-  static constexpr uint32_t kTmemCols = (kOCol + 4 * HG) <= 256 ? 256u : 512u;
+  static constexpr uint32_t kTmemCols = 512u;   // S_a, S_b (2 buffers each) + O^T
 };
 
 // Barrier slots. Every barrier waited on by parity is only ever waited on
 // for a phase that cannot be overtaken by the next one, so the parity test
 // is unambiguous.
 enum Bar {
-  kQFull = 0,      // loader threads -> QK issuer (Q landed)
-  kKvFull = 1,     // 2: loader threads -> QK issuer (tile landed)
+  kQFull = 0,      // loader threads -> QK issuers (Q landed)
+  kKvFull = 1,     // 2: loader threads -> QK issuers (tile landed)
   kKvEmpty = 3,    // 2: PV issuer commit -> loaders (stage free)
-  kSFull = 5,      // 2: QK issuer commit -> softmax (S ready)
-  kPFull = 7,      // 2: softmax threads -> PV issuer, QK issuer (P written, S read)
+  kSFull = 5,      // 2: both QK issuers' commits -> softmax (S ready)
+  kPFull = 7,      // 2: softmax threads -> PV issuer, QK issuers (P written, S read)
   kPvDone = 9,     // PV issuer commit -> softmax (PV of a tile done)
-  kMmaDone = 10,   // 2: each issuer's final drain
-  kNumBars = 12
+  kMmaDone = 10,   // 3: each issuer's final drain
+  kNumBars = 13
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -223,9 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
     *neff_s = 0;
     for (int i = 0; i < kNumBars; ++i) {
       // q_full, kv_full and p_full: one arrival per loader / softmax
-      // thread; the rest: one tcgen05.commit.
+      // thread; s_full: one tcgen05.commit from each QK issuer; the rest:
+      // one tcgen05.commit.
       uint32_t count = 1u;
       if (i == kQFull || i == kPFull || i == kPFull + 1) count = 128u;
+      if (i == kSFull || i == kSFull + 1) count = 2u;
       if (i >= kKvFull && i < kKvFull + kStages) count = 128u;
       mbar_init(&bars[i], count);
     }
@@ -283,6 +289,33 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
         reinterpret_cast<uint16_t*>(vmask + 2 * (2 * i + 1))[pw] = (uint16_t)(ballot >> 16);
       }
     }
+    // Start tile 0 (stage 0) and stream tiles 2 and 3 into L2 right away,
+    // before the block-wide barrier. Entries that are not valid copy zeros,
+    // so this is harmless when the split turns out to be empty.
+    {
+      const uint32_t stage_base = sbase + LY::kKV;
+      const int row_bytes = FP8 ? kRowBytesFp8 : kRowBytesBf16;
+      if constexpr (!FP8) {
+#pragma unroll 4
+        for (int rr = 0; rr < 16; ++rr) {
+          const int64_t g = __shfl_sync(0xffffffffu, grow[0], rr);
+          const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
+          const uint32_t nbytes = g >= 0 ? 16u : 0u;
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const int c = lane + 32 * j;
+            if (c < kChunks)
+              cp_async_16(stage_base + swz_off(pw * 16 + rr, c, kAtomStride), src + c * 16,
+                          nbytes);
+          }
+        }
+        cp_async_commit();
+      }
+      if ((lane >> 4) == 0 && grow[1] >= 0)   // tile 2
+        prefetch_l2_bulk(p.kv + (int64_t)grow[1] * row_bytes, (uint32_t)row_bytes);
+      if ((lane >> 4) == 1 && grow[1] >= 0)   // tile 3
+        prefetch_l2_bulk(p.kv + (int64_t)grow[1] * row_bytes, (uint32_t)row_bytes);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
     if (lane == 0 && last > 0) atomicMax(neff_s, last);
@@ -307,11 +340,23 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
     // ------------------------------------------------------------ producers
     // All four warps fill each tile in turn (16 rows each) into stage t & 1,
     // wait for their own copies (or stores) to land, fence them for the
-    // tensor core and arrive. Q shares the first tile's wait. Right after
-    // tile 0 is under way, every other selected row of the split is streamed
-    // into L2: shared memory holds only two tiles, the L2 (129 MB) holds all
-    // of them, so the HBM reads of later tiles overlap the compute of earlier
-    // ones and their smem copies hit L2.
+    // tensor core and arrive. Q shares the first tile's wait. Shared memory
+    // holds only two tiles, so L2 serves as the deeper stages: while tile t is
+    // copied, the rows of tile t + 3 are streamed into L2 with bulk
+    // prefetches (tiles 2 and 3 at the start), in tile order, so each tile's
+    // HBM reads overlap the compute of the tiles before it and its smem
+    // copies hit L2.
+    // Rows of tile u are held by lanes with (lane >> 4) == (u & 1), slot u >> 1.
+    auto prefetch_tile = [&](int u, int row_bytes) {
+      if (u < n_eff && (lane >> 4) == (u & 1)) {
+        const int sel = u >> 1;
+        const int g = sel == 0 ? grow[0] : sel == 1 ? grow[1] : sel == 2 ? grow[2] : grow[3];
+        if (g >= 0) prefetch_l2_bulk(p.kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
+      }
+    };
+    auto prefetch_ahead = [&](int t, int row_bytes) {
+      if (t >= 1) prefetch_tile(t + 3, row_bytes);   // tiles 2 and 3 went out in the prologue
+    };
 #pragma unroll 1
     for (int t = 0; t < n_eff; ++t) {
       const int stage = t & 1;
@@ -326,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       const int src_lane0 = (t & 1) << 4;
       if constexpr (!FP8) {
 #pragma unroll 4
-        for (int rr = 0; rr < 16; ++rr) {
+        for (int rr = 0; rr < 16 && t > 0; ++rr) {   // tile 0 was issued in the prologue
           const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + rr);
           const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
@@ -339,21 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
           }
         }
         cp_async_commit();
-        if (t == 0) {
-#pragma unroll
-          for (int i = 1; i < 4; ++i)
-            if (grow[i] >= 0)
-              prefetch_l2_bulk(p.kv + (int64_t)grow[i] * kRowBytesBf16, (uint32_t)kRowBytesBf16);
-        }
+        prefetch_ahead(t, kRowBytesBf16);
         cp_async_wait_all();
       } else {
-        if (t == 0) {
-#pragma unroll
-          for (int i = 1; i < 4; ++i)
-            if (grow[i] >= 0)
-              prefetch_l2_bulk(p.kv + (int64_t)grow[i] * kRowBytesFp8, (uint32_t)kRowBytesFp8);
-          cp_async_wait_all();   // Q
-        }
+        prefetch_ahead(t, kRowBytesFp8);
+        if (t == 0) cp_async_wait_all();   // Q
 #pragma unroll 1
         for (int r0 = 0; r0 < 16; r0 += 8) {
           uint2 codes[8][2];
@@ -395,12 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       mbar_arrive(&bars[kKvFull + stage]);
     }
     cp_async_wait_all();
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ QK issuer
-    // QK(t) needs tile t landed and its S buffer free: P(t-2) written means
-    // softmax(t-2) has read S(t-2). Descriptors are precomputed; the 36 MMAs
-    // of a tile are issued back to back.
+  } else if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ QK issuers
+    // Warp 8 accumulates column blocks [0, 5) of QK(t) into S_a, warp 10
+    // blocks [5, 9) into S_b. QK(t) needs tile t landed and its S buffers
+    // free: P(t-2) written means softmax(t-2) has read S(t-2). Descriptors
+    // are precomputed; each issuer's MMAs of a tile go back to back.
     if (lane == 0) {
+      const int a_lo = warp == 8 ? 0 : kQkSplitAtom;
+      const int a_hi = warp == 8 ? kQkSplitAtom : kD / 64;
+      const uint32_t s_col = warp == 8 ? 0u : (uint32_t)kSbCol;
       constexpr uint32_t idesc_qk = make_idesc_bf16(64, kTile, 0, 0);
       const uint64_t q_desc = make_sw128_desc(sbase + LY::kQ, 16, 1024);
       const uint64_t kv_desc0 = make_sw128_desc(sbase + LY::kKV, 16, 1024);
@@ -414,17 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
         }
         tc_fence_after();
         const uint64_t b0 = kv_desc0 + (uint64_t)((sb * kStageBytes) >> 4);
-        const uint32_t d = tmem + sb * kSCols;
+        const uint32_t d = tmem + s_col + sb * kSCols;
+#pragma unroll 1
+        for (int ka = a_lo; ka < a_hi; ++ka) {
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t ka = kk >> 2, off = (kk & 3) * 32;
-          mma_bf16_ss(d, q_desc + ((ka * (HG * 128) + off) >> 4),
-                      b0 + ((ka * kAtomStride + off) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint32_t off = k4 * 32;
+            mma_bf16_ss(d, q_desc + ((ka * (HG * 128) + off) >> 4),
+                        b0 + ((ka * kAtomStride + off) >> 4), idesc_qk,
+                        (ka > a_lo || k4 > 0) ? 1u : 0u);
+          }
         }
         mma_commit(&bars[kSFull + sb]);
       }
-      mma_commit(&bars[kMmaDone]);
-      mbar_wait(&bars[kMmaDone], 0);
+      const int done_bar = kMmaDone + (warp == 8 ? 0 : 2);
+      mma_commit(&bars[done_bar]);
+      mbar_wait(&bars[done_bar], 0);
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -483,7 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       if (ok) {
         tc_fence_after();
         if (warp_has_heads) {
-          tmem_ld16x32bx2_x32_sync(tmem + lane_base + sb * kSCols, s);
+          float s2[32];
+          tmem_ld16x32bx2_x32_pair_sync(tmem + lane_base + sb * kSCols,
+                                        tmem + lane_base + kSbCol + sb * kSCols, s, s2);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j] += s2[j];
           const uint32_t mask = vmask[2 * t + half];
           float mt = -INFINITY;
 #pragma unroll
@@ -558,13 +606,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       float* po = p.part_o + part_base * kDv;
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
-#pragma unroll 1
-        for (int c = 0; c < HG / 16; ++c) {
-          float v[16];
-          tmem_ld16_sync(tmem + lane_base + kOCol + b * HG + 16 * c, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) po[(int64_t)(16 * c + i) * kDv + 128 * b + dv_lane] = v[i];
+        float v[HG];
+        const uint32_t addr = tmem + lane_base + kOCol + b * HG;
+        if constexpr (HG == 64) {
+          tmem_ld64_sync(addr, v);
+        } else if constexpr (HG == 32) {
+          tmem_ld32_sync(addr, v);
+        } else {
+          tmem_ld16_sync(addr, v);
         }
+#pragma unroll
+        for (int i = 0; i < HG; ++i) po[(int64_t)i * kDv + 128 * b + dv_lane] = v[i];
       }
       const float l_other = __shfl_xor_sync(0xffffffffu, l, 16);
       if (active && half == 0) {
@@ -583,6 +635,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
 
 // Merges the splits of one (row, head) in split order: M = max m_s,
 // out = sum 2^(m_s - M) O_s / sum 2^(m_s - M) l_s, lse = (M + log2 L) ln 2.
+// Every split's m, l and O slice is loaded in one round (there are at most
+// kMaxSplits) before any arithmetic, so the loads overlap.
+constexpr int kMaxSplits = 2048 / kSplitEntries;
+
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
                                                       const float* __restrict__ part_m,
                                                       const float* __restrict__ part_l,
@@ -592,8 +648,22 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   const int64_t rh = blockIdx.x;  // row * H + h
   const int t = threadIdx.x;
   const int64_t RH = R * H;
+  float ms[kMaxSplits], ls[kMaxSplits];
+  float4 os[kMaxSplits];
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) {
+    ms[s] = -INFINITY;
+    ls[s] = 0.0f;
+    os[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (s < S) {
+      ms[s] = part_m[s * RH + rh];
+      ls[s] = part_l[s * RH + rh];
+      os[s] = *reinterpret_cast<const float4*>(part_o + (s * RH + rh) * kDv + 4 * t);
+    }
+  }
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[s * RH + rh]);
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ms[s]);
   __nv_bfloat16* o = out + rh * kDv + 4 * t;
   if (M == -INFINITY) {
     *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
@@ -602,16 +672,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   }
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float L = 0.0f;
-  for (int s = 0; s < S; ++s) {
-    const float ms = part_m[s * RH + rh];
-    if (ms == -INFINITY) continue;
-    const float w = ex2(ms - M);
-    L += w * part_l[s * RH + rh];
-    const float4 v = *reinterpret_cast<const float4*>(part_o + (s * RH + rh) * kDv + 4 * t);
-    acc[0] += w * v.x;
-    acc[1] += w * v.y;
-    acc[2] += w * v.z;
-    acc[3] += w * v.w;
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) {
+    if (ms[s] == -INFINITY) continue;   // empty split (its O slice is never read)
+    const float w = ex2(ms[s] - M);
+    L += w * ls[s];
+    acc[0] += w * os[s].x;
+    acc[1] += w * os[s].y;
+    acc[2] += w * os[s].z;
+    acc[3] += w * os[s].w;
   }
   const float inv = 1.0f / L;
   uint2 r;

@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
   const float* __restrict__ p = scores + row * stride + s + c0;
   const bool aligned = (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
 
-  for (int i = tid; i < kBins; i += kThreads) hist[0][i] = 0u;
+  for (int i = tid; i < kBins; i += kThreads) {
+    hist[0][i] = 0u;
+    hist[1][i] = 0u;
+  }
   __syncthreads();
 
   // Load the chunk (8 x 16 B per thread in flight), store keys, histogram
@@ -378,10 +381,12 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
     const uint32_t nbins = 1u << width;
     const int buf = pass & 1;
     if (pass > 0) {
-      // hist[buf] was last read by the other CTAs two passes ago, before the
-      // previous pass's cluster barrier.
-      for (int i = tid; i < kBins; i += kThreads) hist[buf][i] = 0u;
-      __syncthreads();
+      if (pass == 2) {
+        // hist[0] was last read by the other CTAs in pass 0, before the
+        // cluster barrier of pass 1. (hist[1] starts out zeroed.)
+        for (int i = tid; i < kBins; i += kThreads) hist[0][i] = 0u;
+        __syncthreads();
+      }
       for (int i = tid; i < n; i += kThreads) {
         const uint32_t kk = keys[i];
         if ((kk >> shift) == prefix) atomicAdd(&hist[buf][(kk >> nshift) & (nbins - 1u)], 1u);
@@ -471,13 +476,28 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
   }
   __syncthreads();
   cluster_sync_all();
-  uint32_t carry_gt = 0u, carry_eq = 0u;
-  for (uint32_t r = 0; r < crank; ++r) {
-    carry_gt += dsmem_ld(&cta_tot[0], r);
-    carry_eq += dsmem_ld(&cta_tot[1], r);
+  // Carry-in of this chunk: the totals of the lower-ranked CTAs, read in
+  // parallel by warp 0 and shared through shared memory.
+  __shared__ uint32_t carry[2];
+  if (warp == 0) {
+    uint32_t cg = 0u, ce = 0u;
+    if ((uint32_t)lane < crank) {
+      cg = dsmem_ld(&cta_tot[0], (uint32_t)lane);
+      ce = dsmem_ld(&cta_tot[1], (uint32_t)lane);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cg += __shfl_xor_sync(0xffffffffu, cg, o);
+      ce += __shfl_xor_sync(0xffffffffu, ce, o);
+    }
+    if (lane == 0) {
+      carry[0] = cg;
+      carry[1] = ce;
+    }
   }
-  uint32_t g = carry_gt + wcount[warp][0];
-  uint32_t qe = carry_eq + wcount[warp][1];
+  __syncthreads();
+  uint32_t g = carry[0] + wcount[warp][0];
+  uint32_t qe = carry[1] + wcount[warp][1];
   const uint32_t lt_mask = (1u << lane) - 1u;
   for (int i0 = w0; i0 < w1; i0 += 32) {
     const int i = i0 + lane;
