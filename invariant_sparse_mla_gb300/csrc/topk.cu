@@ -49,10 +49,12 @@ __device__ __forceinline__ uint32_t score_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block-wide prefix sum of one uint32 per thread; `total` gets the
-// block sum. Ends with a barrier so `buf` may be reused right away.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* buf,
-                                                         uint32_t& total) {
+// Exclusive block-wide prefix sum of one uint32 per thread (NT threads);
+// `total` gets the block sum. Ends with a barrier so `buf` may be reused.
+template <int NT>
+__device__ __forceinline__ uint32_t block_exclusive_scan_nt(uint32_t v, uint32_t* buf,
+                                                            uint32_t& total) {
+  constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
@@ -76,6 +78,11 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* b
   total = buf[kWarps - 1];
   __syncthreads();
   return before + x - v;
+}
+
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* buf,
+                                                         uint32_t& total) {
+  return block_exclusive_scan_nt<kThreads>(v, buf, total);
 }
 
 // Loads elements [i0, i0 + 4) of the row (those below L) as keys; `valid`
@@ -519,11 +526,268 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
   cluster_sync_all();
 }
 
+
+// ---------------------------------------------------------------------------
+// Streaming variant for many rows of up to 65536 scores: one CTA per row, no
+// cluster. The row is read from global memory once; while it streams in,
+// each key's top 16 bits go to shared memory (2 bytes per score, 128 KB for
+// the longest row) and a histogram of its top 12 bits is built. A second
+// pass over shared memory refines the threshold to 16 bits. Only if the
+// threshold bucket still holds more keys than needed are the low 16 bits
+// read back from global memory (L2-resident by then), for the keys of that
+// bucket alone, in two 8-bit passes. The ordered compaction reads the
+// prefixes from shared memory and re-reads full keys only for that bucket.
+
+constexpr int kStreamThreads = 1024;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamMaxLen = 65536;
+constexpr int kStreamBins = 4096;   // top 12 key bits
+constexpr int kStreamBinsPerThread = kStreamBins / kStreamThreads;
+constexpr int64_t kStreamMinRows = 256;   // below this the cluster kernel spreads a row wider
+
+// Picks, among `nbins` bins counted in `hist` (descending bin order), the bin
+// holding the `take`-th largest key. Every thread returns the same (bin,
+// count of that bin, take within that bin).
+__device__ __forceinline__ void stream_pick(const uint32_t* hist, int nbins, uint32_t take,
+                                            uint32_t* scan_buf, uint32_t* pick, uint32_t& bin,
+                                            uint32_t& cnt, uint32_t& take_in_bin) {
+  const int tid = threadIdx.x;
+  uint32_t c[kStreamBinsPerThread];
+  uint32_t mine = 0u;
+#pragma unroll
+  for (int q = 0; q < kStreamBinsPerThread; ++q) {
+    const int b = nbins - 1 - (tid * kStreamBinsPerThread + q);
+    c[q] = b >= 0 ? hist[b] : 0u;
+    mine += c[q];
+  }
+  uint32_t total;
+  uint32_t above = block_exclusive_scan_nt<kStreamThreads>(mine, scan_buf, total);
+#pragma unroll
+  for (int q = 0; q < kStreamBinsPerThread; ++q) {
+    const int b = nbins - 1 - (tid * kStreamBinsPerThread + q);
+    if (b >= 0 && above < take && take <= above + c[q]) {
+      pick[0] = (uint32_t)b;
+      pick[1] = take - above;
+      pick[2] = c[q];
+    }
+    above += c[q];
+  }
+  __syncthreads();
+  bin = pick[0];
+  take_in_bin = pick[1];
+  cnt = pick[2];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(
+    const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ starts,
+    const int32_t* __restrict__ ends, int k, int32_t* __restrict__ out) {
+  extern __shared__ __align__(16) uint16_t pre[];   // top 16 key bits of each score
+  __shared__ uint32_t hist[kStreamBins];
+  __shared__ uint32_t scan_buf[32];
+  __shared__ uint32_t pick[3];
+  __shared__ uint32_t wcount[kStreamWarps][2];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const int64_t s = starts[row];
+  const int64_t e = ends[row];
+  int64_t L64 = 0;
+  if (s >= 0 && s <= stride) {
+    L64 = e - s;
+    if (L64 < 0) L64 = 0;
+    if (L64 > stride - s) L64 = stride - s;
+  }
+  int32_t* __restrict__ orow = out + row * (int64_t)k;
+  if (L64 <= (int64_t)k) {
+    for (int j = tid; j < k; j += kStreamThreads) orow[j] = (int64_t)j < L64 ? j : -1;
+    return;
+  }
+  const int L = (int)L64;   // <= kStreamMaxLen
+  const float* __restrict__ p = scores + row * stride + s;
+  const bool aligned = (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
+
+  for (int i = tid; i < kStreamBins; i += kStreamThreads) hist[i] = 0u;
+  __syncthreads();
+
+  // Pass A: stream the row (8 x 16 bytes per thread in flight), keep the top
+  // 16 key bits, histogram the top 12.
+  if (aligned) {
+    const int n4 = L >> 2;
+    const float4* p4 = reinterpret_cast<const float4*>(p);
+    for (int base = 0; base < n4; base += 8 * kStreamThreads) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kStreamThreads + tid;
+        if (i < n4) v[u] = p4[i];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kStreamThreads + tid;
+        if (i < n4) {
+          const uint32_t k0 = score_key(v[u].x), k1 = score_key(v[u].y);
+          const uint32_t k2 = score_key(v[u].z), k3 = score_key(v[u].w);
+          reinterpret_cast<uint2*>(pre)[i] =
+              make_uint2((k0 >> 16) | (k1 & 0xFFFF0000u), (k2 >> 16) | (k3 & 0xFFFF0000u));
+          atomicAdd(&hist[k0 >> 20], 1u);
+          atomicAdd(&hist[k1 >> 20], 1u);
+          atomicAdd(&hist[k2 >> 20], 1u);
+          atomicAdd(&hist[k3 >> 20], 1u);
+        }
+      }
+    }
+    for (int i = (n4 << 2) + tid; i < L; i += kStreamThreads) {
+      const uint32_t kk = score_key(p[i]);
+      pre[i] = (uint16_t)(kk >> 16);
+      atomicAdd(&hist[kk >> 20], 1u);
+    }
+  } else {
+    for (int base = 0; base < L; base += 8 * kStreamThreads) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kStreamThreads + tid;
+        if (i < L) v[u] = p[i];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kStreamThreads + tid;
+        if (i < L) {
+          const uint32_t kk = score_key(v[u]);
+          pre[i] = (uint16_t)(kk >> 16);
+          atomicAdd(&hist[kk >> 20], 1u);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // Threshold: prefix P of the key at `shift` resolved bits, `take` of the
+  // keys equal to it are selected (the lowest positions).
+  uint32_t take = (uint32_t)k, P, cnt, b;
+  int shift = 20;
+  stream_pick(hist, kStreamBins, take, scan_buf, pick, P, cnt, take);
+  if (cnt != take) {
+    // Pass B (shared memory only): next 4 bits among keys with prefix P.
+    if (tid < 16) hist[tid] = 0u;
+    __syncthreads();
+    for (int i = tid; i < L; i += kStreamThreads) {
+      const uint32_t v = pre[i];
+      if ((v >> 4) == P) atomicAdd(&hist[v & 15u], 1u);
+    }
+    __syncthreads();
+    stream_pick(hist, 16, take, scan_buf, pick, b, cnt, take);
+    P = (P << 4) | b;
+    shift = 16;
+    // Passes C and D: low 16 bits, read back for the keys of bucket P only.
+    for (int pass = 0; pass < 2 && cnt != take; ++pass) {
+      const int nshift = shift - 8;
+      if (tid < 256) hist[tid] = 0u;
+      __syncthreads();
+      for (int i = tid; i < L; i += kStreamThreads) {
+        if ((uint32_t)pre[i] == (P >> (16 - shift))) {
+          const uint32_t kk = score_key(p[i]);
+          if ((kk >> shift) == P) atomicAdd(&hist[(kk >> nshift) & 255u], 1u);
+        }
+      }
+      __syncthreads();
+      stream_pick(hist, 256, take, scan_buf, pick, b, cnt, take);
+      P = (P << 8) | b;
+      shift = nshift;
+    }
+  }
+
+  // Ordered compaction: warp w owns the contiguous segment [w*seg, w*seg+seg).
+  const uint32_t p16 = P >> (shift >= 16 ? 0 : 16 - shift);   // bucket at 16 bits
+  auto classify = [&](int i, bool& gt, bool& eq) {
+    const uint32_t v = pre[i];
+    if (shift >= 16) {
+      const uint32_t hi = v >> (shift - 16);
+      gt = hi > P;
+      eq = hi == P;
+    } else if (v != p16) {
+      gt = v > p16;
+      eq = false;
+    } else {
+      const uint32_t hi = score_key(p[i]) >> shift;
+      gt = hi > P;
+      eq = hi == P;
+    }
+  };
+  const int seg = ((L + kStreamWarps - 1) / kStreamWarps + 31) & ~31;
+  const int w0 = warp * seg;
+  const int w1 = min(L, w0 + seg);
+  uint32_t ngt = 0u, neq = 0u;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    bool gt = false, eq = false;
+    if (i < w1) classify(i, gt, eq);
+    ngt += __popc(__ballot_sync(0xffffffffu, gt));
+    neq += __popc(__ballot_sync(0xffffffffu, eq));
+  }
+  if (lane == 0) {
+    wcount[warp][0] = ngt;
+    wcount[warp][1] = neq;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t cg = wcount[lane][0], ce = wcount[lane][1];
+    const uint32_t og = cg, oe = ce;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t yg = __shfl_up_sync(0xffffffffu, cg, o);
+      const uint32_t ye = __shfl_up_sync(0xffffffffu, ce, o);
+      if (lane >= o) {
+        cg += yg;
+        ce += ye;
+      }
+    }
+    wcount[lane][0] = cg - og;   // exclusive
+    wcount[lane][1] = ce - oe;
+  }
+  __syncthreads();
+  uint32_t g = wcount[warp][0];
+  uint32_t qe = wcount[warp][1];
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    bool gt = false, eq = false;
+    if (i < w1) classify(i, gt, eq);
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt);
+    const uint32_t be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t my_g = g + __popc(bg & lt_mask);
+    const uint32_t my_e = qe + __popc(be & lt_mask);
+    if (gt) orow[my_g + min(my_e, take)] = i;
+    else if (eq && my_e < take) orow[my_g + my_e] = i;
+    g += __popc(bg);
+    qe += __popc(be);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const int32_t* starts,
                         const int32_t* ends, int k, int32_t* out, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
+  // Many rows of up to 64K scores: one streaming CTA per row. Fewer rows
+  // (or longer ones): a cluster per row, so that one row's work is spread
+  // over several SMs. The selected set is unique, so the kernel choice never
+  // changes the output.
+  if (stride <= kStreamMaxLen && rows >= kStreamMinRows) {
+    const size_t smem = ((size_t)stride * sizeof(uint16_t) + 15) & ~size_t(15);
+    static std::atomic<bool> stream_attr{false};
+    if (!stream_attr.load(std::memory_order_acquire)) {
+      cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)(kStreamMaxLen * sizeof(uint16_t)));
+      if (e != cudaSuccess) return e;
+      stream_attr.store(true, std::memory_order_release);
+    }
+    topk_stream_kernel<<<(unsigned)rows, kStreamThreads, smem, stream>>>(scores, stride, starts,
+                                                                         ends, k, out);
+    return cudaGetLastError();
+  }
   // Cluster size from the row stride alone: about 8K keys per CTA, at most 8
   // CTAs. Rows longer than 8 x 16K keys take the single-CTA kernel.
   int64_t C = (stride + 8191) / 8192;

@@ -168,3 +168,63 @@ def test_run_to_run_deterministic(ds):
     a = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)
     b = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)
     assert torch.equal(a, b)
+
+
+def _mixed_rows(rng, R, stride, k):
+    """R rows cycling through the cases that stress each refinement pass."""
+    s = np.empty((R, stride), np.float32)
+    starts, ends = np.zeros(R, np.int64), np.full(R, stride, np.int64)
+    specials = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan], np.float32)
+    for r in range(R):
+        case = r % 9
+        if case == 0:
+            s[r] = np.round(rng.standard_normal(stride) * 8) / 8
+        elif case == 1:  # eight values: the threshold bucket is unresolved at 32 bits
+            s[r] = rng.integers(0, 8, stride)
+        elif case == 2:
+            s[r] = 1.5
+        elif case == 3:
+            s[r] = rng.choice(specials, stride)
+        elif case == 4:  # every score shares its top 16 key bits
+            s[r] = 1.0 + rng.random(stride) * 2.0 ** -7
+        elif case == 5:  # shared top 16 bits, ties in the low 8 bits
+            s[r] = 1.0 + rng.integers(0, 64, stride) * 2.0 ** -14
+        elif case == 6:  # row no longer than k: no score is read
+            s[r] = rng.standard_normal(stride)
+            ends[r] = int(rng.integers(0, k + 1))
+        elif case == 7:  # odd start and end
+            s[r] = rng.standard_normal(stride)
+            starts[r] = int(rng.integers(1, 40))
+            ends[r] = stride - int(rng.integers(0, 40))
+        else:
+            s[r] = rng.standard_normal(stride) * 1e-3
+    return s, starts, ends
+
+
+@pytest.mark.parametrize("stride,k", [(20000, 2048), (20001, 700), (9000, 64)])
+def test_many_rows_mixed_cases_exact(ds, stride, k):
+    # At least 256 rows of at most 64K scores: one CTA per row streams the row.
+    rng = np.random.default_rng(stride + k)
+    s, a, b = _mixed_rows(rng, 288, stride, k)
+    check(ds, s, a, b, k)
+
+
+def test_many_rows_longest_rows_sampled(ds):
+    rng = np.random.default_rng(11)
+    R, stride, k = 256, 65536, 2048
+    s, a, b = _mixed_rows(rng, R, stride, k)
+    got = run(ds, s, a, b, k)
+    rows = list(range(18)) + rng.choice(R, 12, replace=False).tolist()
+    want = oracle.topk_per_row(s[rows], a[rows], b[rows], k)
+    assert np.array_equal(got[rows], want)
+
+
+def test_stream_and_cluster_kernels_agree(ds):
+    # The same rows alone (a cluster per row) and inside a batch of 300 rows
+    # (one streaming CTA per row) give identical indices.
+    rng = np.random.default_rng(12)
+    s, a, b = _mixed_rows(rng, 300, 30000, 2048)
+    big = run(ds, s, a, b, 2048)
+    for r in [0, 1, 3, 4, 5, 7, 8, 299]:
+        one = run(ds, s[r:r + 1], a[r:r + 1], b[r:r + 1], 2048)[0]
+        assert np.array_equal(one, big[r]), r
