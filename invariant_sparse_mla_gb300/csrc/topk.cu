@@ -528,43 +528,71 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
 
 
 // ---------------------------------------------------------------------------
-// Streaming variant for many rows of up to 65536 scores: one CTA per row, no
-// cluster. The row is read from global memory once; while it streams in,
-// each key's top 16 bits go to shared memory (2 bytes per score, 128 KB for
-// the longest row) and a histogram of its top 12 bits is built. A second
-// pass over shared memory refines the threshold to 16 bits. Only if the
-// threshold bucket still holds more keys than needed are the low 16 bits
-// read back from global memory (L2-resident by then), for the keys of that
-// bucket alone, in two 8-bit passes. The ordered compaction reads the
-// prefixes from shared memory and re-reads full keys only for that bucket.
+// Rows of up to 32768 scores: one 1024-thread CTA per row, the whole row in
+// shared memory. Every thread issues asynchronous 16-byte copies for its
+// share of the row (4-byte copies when the row start is not 16-byte
+// aligned), so the full row is in flight at once without holding registers.
+// The keys are formed in place while the 12-bit histogram is built; the low
+// 20 bits of the threshold are resolved by 8-, 8- and 4-bit histogram passes
+// over shared memory that count only keys still tied with the threshold
+// prefix. One more pass writes the selection as a bitmap (eight lanes share a
+// 32-position word), ties at the full key go to the lowest positions by a
+// prefix count over the tied-key bitmap, and thread t turns bitmap word t
+// into output slots after one block-wide scan.
 
-constexpr int kStreamThreads = 1024;
-constexpr int kStreamWarps = kStreamThreads / 32;
-constexpr int kStreamMaxLen = 65536;
-constexpr int kStreamBins = 4096;   // top 12 key bits
-constexpr int kStreamBinsPerThread = kStreamBins / kStreamThreads;
-constexpr int64_t kStreamMinRows = 256;   // below this the cluster kernel spreads a row wider
+constexpr int kRowThreads = 1024;
+constexpr int kRowMaxLen = 32768;
+constexpr int kRowWords = kRowMaxLen / 32;   // one per thread
+constexpr int kRowBins = 4096;
+
+struct RowSmem {
+  uint32_t key[kRowMaxLen];
+  uint32_t hist[kRowBins];
+  uint32_t sel[kRowWords];
+  uint32_t eqb[kRowWords];
+  uint32_t hsmall[256];
+  uint32_t scan_buf[32];
+  uint32_t pick[3];
+};
+
+__device__ __forceinline__ void cp_async_16B(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_4B(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
 
 // Picks, among `nbins` bins counted in `hist` (descending bin order), the bin
-// holding the `take`-th largest key. Every thread returns the same (bin,
-// count of that bin, take within that bin).
-__device__ __forceinline__ void stream_pick(const uint32_t* hist, int nbins, uint32_t take,
-                                            uint32_t* scan_buf, uint32_t* pick, uint32_t& bin,
-                                            uint32_t& cnt, uint32_t& take_in_bin) {
+// holding the `take`-th largest key: every thread gets (bin, count of that
+// bin, take within that bin). Bins per thread: ceil(4096 / NT).
+template <int NT>
+__device__ __forceinline__ void block_pick(const uint32_t* hist, int nbins, uint32_t take,
+                                           uint32_t* scan_buf, uint32_t* pick, uint32_t& bin,
+                                           uint32_t& cnt, uint32_t& take_in_bin) {
+  constexpr int kPer = (4096 + NT - 1) / NT;
   const int tid = threadIdx.x;
-  uint32_t c[kStreamBinsPerThread];
+  uint32_t c[kPer];
   uint32_t mine = 0u;
 #pragma unroll
-  for (int q = 0; q < kStreamBinsPerThread; ++q) {
-    const int b = nbins - 1 - (tid * kStreamBinsPerThread + q);
+  for (int q = 0; q < kPer; ++q) {
+    const int b = nbins - 1 - (tid * kPer + q);
     c[q] = b >= 0 ? hist[b] : 0u;
     mine += c[q];
   }
   uint32_t total;
-  uint32_t above = block_exclusive_scan_nt<kStreamThreads>(mine, scan_buf, total);
+  uint32_t above = block_exclusive_scan_nt<NT>(mine, scan_buf, total);
 #pragma unroll
-  for (int q = 0; q < kStreamBinsPerThread; ++q) {
-    const int b = nbins - 1 - (tid * kStreamBinsPerThread + q);
+  for (int q = 0; q < kPer; ++q) {
+    const int b = nbins - 1 - (tid * kPer + q);
     if (b >= 0 && above < take && take <= above + c[q]) {
       pick[0] = (uint32_t)b;
       pick[1] = take - above;
@@ -579,189 +607,519 @@ __device__ __forceinline__ void stream_pick(const uint32_t* hist, int nbins, uin
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(
+// Mask of the first m set bits of x.
+__device__ __forceinline__ uint32_t first_set_bits(uint32_t x, uint32_t m) {
+  uint32_t r = 0u;
+  while (m-- > 0u && x) {
+    const uint32_t low = x & (0u - x);
+    r |= low;
+    x ^= low;
+  }
+  return r;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 1) topk_smem_kernel(
     const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ starts,
     const int32_t* __restrict__ ends, int k, int32_t* __restrict__ out) {
-  extern __shared__ __align__(16) uint16_t pre[];   // top 16 key bits of each score
-  __shared__ uint32_t hist[kStreamBins];
-  __shared__ uint32_t scan_buf[32];
-  __shared__ uint32_t pick[3];
-  __shared__ uint32_t wcount[kStreamWarps][2];
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  extern __shared__ __align__(16) unsigned char row_smem_raw[];
+  RowSmem& sm = *reinterpret_cast<RowSmem*>(row_smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31;
   const int64_t row = blockIdx.x;
   const int64_t s = starts[row];
   const int64_t e = ends[row];
-  int64_t L64 = 0;
+  int L = 0;
   if (s >= 0 && s <= stride) {
-    L64 = e - s;
+    int64_t L64 = e - s;
     if (L64 < 0) L64 = 0;
     if (L64 > stride - s) L64 = stride - s;
+    L = (int)L64;   // <= kRowMaxLen
   }
   int32_t* __restrict__ orow = out + row * (int64_t)k;
-  if (L64 <= (int64_t)k) {
-    for (int j = tid; j < k; j += kStreamThreads) orow[j] = (int64_t)j < L64 ? j : -1;
+  if (L <= k) {   // every position is selected; no score is read
+    for (int j = tid; j < k; j += kRowThreads) orow[j] = j < L ? j : -1;
     return;
   }
-  const int L = (int)L64;   // <= kStreamMaxLen
   const float* __restrict__ p = scores + row * stride + s;
-  const bool aligned = (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
 
-  for (int i = tid; i < kStreamBins; i += kStreamThreads) hist[i] = 0u;
+  // The whole row in flight. Key slot i holds position i; slots from L up to
+  // the next multiple of 4 hold bytes of the same 16-byte granules and are
+  // never counted or selected.
+  const int n4 = (L + 3) >> 2;
+  if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0u) {
+    for (int j = tid; j < n4; j += kRowThreads) cp_async_16B(&sm.key[4 * j], p + 4 * j);
+  } else {
+    for (int i = tid; i < L; i += kRowThreads) cp_async_4B(&sm.key[i], p + i);
+  }
+  for (int i = tid; i < kRowBins; i += kRowThreads) sm.hist[i] = 0u;
+  sm.sel[tid] = 0u;
+  sm.eqb[tid] = 0u;
+  cp_async_commit_wait_all();
   __syncthreads();
 
-  // Pass A: stream the row (8 x 16 bytes per thread in flight), keep the top
-  // 16 key bits, histogram the top 12.
-  if (aligned) {
-    const int n4 = L >> 2;
-    const float4* p4 = reinterpret_cast<const float4*>(p);
-    for (int base = 0; base < n4; base += 8 * kStreamThreads) {
-      float4 v[8];
+  // Keys in place, and the histogram of their top 12 bits.
+  uint4* const key4 = reinterpret_cast<uint4*>(sm.key);
+  for (int j = tid; j < n4; j += kRowThreads) {
+    uint4 w = key4[j];
+    w.x = score_key(__uint_as_float(w.x));
+    w.y = score_key(__uint_as_float(w.y));
+    w.z = score_key(__uint_as_float(w.z));
+    w.w = score_key(__uint_as_float(w.w));
+    key4[j] = w;
+    const int valid = min(4, L - 4 * j);
+    atomicAdd(&sm.hist[w.x >> 20], 1u);
+    if (valid > 1) atomicAdd(&sm.hist[w.y >> 20], 1u);
+    if (valid > 2) atomicAdd(&sm.hist[w.z >> 20], 1u);
+    if (valid > 3) atomicAdd(&sm.hist[w.w >> 20], 1u);
+  }
+  __syncthreads();
+
+  // Threshold state: `P` is the threshold key's prefix with `shift` low bits
+  // dropped; `take` of the `cnt` keys with that prefix (the lowest positions)
+  // are selected.
+  uint32_t take = (uint32_t)k, P, cnt, b;
+  block_pick<kRowThreads>(sm.hist, kRowBins, take, sm.scan_buf, sm.pick, P, cnt, take);
+  int shift = 20;
+  for (int pass = 0; pass < 3 && cnt != take; ++pass) {
+    const int width = pass < 2 ? 8 : 4;
+    const int nshift = shift - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    if (tid < 256) sm.hsmall[tid] = 0u;
+    __syncthreads();
+    for (int j = tid; j < n4; j += kRowThreads) {
+      const uint4 w = key4[j];
+      const int valid = min(4, L - 4 * j);
+      if ((w.x >> shift) == P) atomicAdd(&sm.hsmall[(w.x >> nshift) & dmask], 1u);
+      if (valid > 1 && (w.y >> shift) == P) atomicAdd(&sm.hsmall[(w.y >> nshift) & dmask], 1u);
+      if (valid > 2 && (w.z >> shift) == P) atomicAdd(&sm.hsmall[(w.z >> nshift) & dmask], 1u);
+      if (valid > 3 && (w.w >> shift) == P) atomicAdd(&sm.hsmall[(w.w >> nshift) & dmask], 1u);
+    }
+    __syncthreads();
+    block_pick<kRowThreads>(sm.hsmall, 1 << width, take, sm.scan_buf, sm.pick, b, cnt, take);
+    P = (P << width) | b;
+    shift = nshift;
+  }
+
+  // Selection bitmap: lanes 8m..8m+7 of a warp hold the 32 positions of one
+  // word; their nibbles are OR-ed together and lane 8m stores the word.
+  const bool all_eq = cnt == take;
+  for (int j0 = 0; j0 < n4; j0 += kRowThreads) {
+    const int j = j0 + tid;
+    uint32_t gt = 0u, eq = 0u;
+    if (j < n4) {
+      const uint4 w = key4[j];
+      const uint32_t kk[4] = {w.x, w.y, w.z, w.w};
+      const int valid = min(4, L - 4 * j);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kStreamThreads + tid;
-        if (i < n4) v[u] = p4[i];
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t hi = kk[q] >> shift;
+        if (q < valid) {
+          gt |= (hi > P || (all_eq && hi == P) ? 1u : 0u) << q;
+          eq |= (!all_eq && hi == P ? 1u : 0u) << q;
+        }
       }
+    }
+    const int sh = 4 * (lane & 7);
+    gt <<= sh;
+    eq <<= sh;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+    for (int o = 1; o < 8; o <<= 1) {
+      gt |= __shfl_xor_sync(0xffffffffu, gt, o);
+      eq |= __shfl_xor_sync(0xffffffffu, eq, o);
+    }
+    if ((lane & 7) == 0 && j < n4) {
+      sm.sel[j >> 3] = gt;
+      sm.eqb[j >> 3] = eq;
+    }
+  }
+  __syncthreads();
+
+  // Thread t owns word t: positions [32t, 32t + 32).
+  uint32_t w = sm.sel[tid];
+  if (!all_eq) {
+    // Keys equal at all 32 bits: the lowest `take` positions win.
+    const uint32_t eqw = sm.eqb[tid];
+    uint32_t tot;
+    const uint32_t r = block_exclusive_scan_nt<kRowThreads>(__popc(eqw), sm.scan_buf, tot);
+    if (r < take) w |= first_set_bits(eqw, take - r);
+  }
+  uint32_t total;
+  uint32_t pos = block_exclusive_scan_nt<kRowThreads>(__popc(w), sm.scan_buf, total);
+  while (w) {
+    const int bit = __ffs(w) - 1;
+    w &= w - 1u;
+    if (pos < (uint32_t)k) orow[pos] = 32 * tid + bit;
+    ++pos;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Streaming variant for many rows of up to 65536 scores: a persistent grid of
+// two 512-thread CTAs per SM walks the rows, so that one CTA's resolution
+// work overlaps the other's loads.
+//
+// Pass A streams the row once from global memory, builds a histogram of the
+// keys' top 12 bits and appends every key whose 12-bit prefix is at least a
+// guess G to a candidate list (position and key). G is one bin below the
+// threshold bin of the CTA's previous row, so for rows of similar score
+// distributions the list holds every selected key plus a few hundred more.
+// Once the threshold bin P is known, the list is valid if G <= P and it did
+// not overflow; otherwise a second pass re-reads the row (now in L2) and
+// collects the members of bin P alone, marking keys above it directly in the
+// selection bitmap. The low 20 bits of the threshold are then resolved on the
+// list in 8-, 8- and 4-bit histogram passes; a bin too large for the list is
+// resolved by passes over the row in global memory instead. The guess only
+// decides how much work a row takes: the selected set is always exact.
+//
+// The selection is a bitmap of the row's positions. Keys tied at all 32 bits
+// with the threshold go to the lowest positions, ranked by a prefix count
+// over a bitmap of the tied keys. Each thread owns 128 consecutive positions
+// (4 words), so one block-wide scan of per-thread counts gives every output
+// slot in index order.
+
+constexpr int kStreamThreads = 512;
+constexpr int kStreamCtasPerSm = 2;
+constexpr int kStreamVec = 4;   // 16-byte loads per thread in flight
+constexpr int kStreamMaxLen = 65536;
+constexpr int kStreamBins = 4096;                      // top 12 key bits
+constexpr int kStreamBinsPerThread = kStreamBins / kStreamThreads;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamSeg = 512;                        // list entries per warp
+constexpr int kStreamWords = kStreamMaxLen / 32;       // one bit per position
+constexpr int kStreamWordsPerThread = kStreamWords / kStreamThreads;
+constexpr uint32_t kStreamNoGuess = kStreamBins;       // collects nothing
+constexpr int64_t kStreamMinRows = 256;   // below this the cluster kernel spreads a row wider
+
+struct StreamSmem {
+  uint32_t hist[kStreamBins];
+  uint32_t cand_idx[kStreamWarps * kStreamSeg];   // warp w appends to [w * kStreamSeg, ...)
+  uint32_t cand_key[kStreamWarps * kStreamSeg];
+  uint32_t sel[kStreamWords];   // selected positions
+  uint32_t eqb[kStreamWords];   // positions tied with the threshold key
+  uint32_t hsmall[256];
+  uint32_t scan_buf[32];
+  uint32_t pick[3];
+  uint32_t nseg[kStreamWarps];   // entries in each warp's segment
+  uint32_t overflow;            // some segment was full
+};
+
+// Picks, among `nbins` bins counted in `hist` (descending bin order), the bin
+// holding the `take`-th largest key. Every thread returns the same (bin,
+// count of that bin, take within that bin).
+__device__ __forceinline__ void stream_pick(const uint32_t* hist, int nbins, uint32_t take,
+                                            StreamSmem& sm, uint32_t& bin, uint32_t& cnt,
+                                            uint32_t& take_in_bin) {
+  const int tid = threadIdx.x;
+  uint32_t c[kStreamBinsPerThread];
+  uint32_t mine = 0u;
+#pragma unroll
+  for (int q = 0; q < kStreamBinsPerThread; ++q) {
+    const int b = nbins - 1 - (tid * kStreamBinsPerThread + q);
+    c[q] = b >= 0 ? hist[b] : 0u;
+    mine += c[q];
+  }
+  uint32_t total;
+  uint32_t above = block_exclusive_scan_nt<kStreamThreads>(mine, sm.scan_buf, total);
+#pragma unroll
+  for (int q = 0; q < kStreamBinsPerThread; ++q) {
+    const int b = nbins - 1 - (tid * kStreamBinsPerThread + q);
+    if (b >= 0 && above < take && take <= above + c[q]) {
+      sm.pick[0] = (uint32_t)b;
+      sm.pick[1] = take - above;
+      sm.pick[2] = c[q];
+    }
+    above += c[q];
+  }
+  __syncthreads();
+  bin = sm.pick[0];
+  take_in_bin = sm.pick[1];
+  cnt = sm.pick[2];
+  __syncthreads();
+}
+
+// Clamped [start, end) of a row, as in every other kernel here: the length
+// is end - start, bounded to [0, stride - start]; a start outside [0,
+// stride] gives an empty row.
+__device__ __forceinline__ int stream_row_len(const int32_t* starts, const int32_t* ends,
+                                              int64_t row, int64_t stride, int64_t& s) {
+  s = starts[row];
+  const int64_t e = ends[row];
+  int64_t L = 0;
+  if (s >= 0 && s <= stride) {
+    L = e - s;
+    if (L < 0) L = 0;
+    if (L > stride - s) L = stride - s;
+  }
+  return (int)L;
+}
+
+
+// First slot, in the warp's own list segment, for this thread's `n` appends;
+// `used` (the same in every lane) is the segment's fill. Every lane of the
+// warp must call it.
+__device__ __forceinline__ uint32_t stream_reserve(uint32_t n, uint32_t& used) {
+  const int lane = threadIdx.x & 31;
+  uint32_t incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t slot = used + incl - n;
+  used += __shfl_sync(0xffffffffu, incl, 31);
+  return slot;
+}
+
+// One streaming pass over the row's keys, kStreamVec x 16 bytes per thread in
+// flight.
+// kFirst: histogram of the top 12 bits; keys with prefix >= bin are listed.
+// Otherwise: keys with prefix > bin are marked in `sel`, those equal listed.
+template <bool kFirst>
+__device__ __forceinline__ void stream_pass(const float* __restrict__ p, int L, uint32_t bin,
+                                            StreamSmem& sm) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  uint32_t used = 0u;   // this warp's segment fill
+  uint32_t* const seg_idx = sm.cand_idx + warp * kStreamSeg;
+  uint32_t* const seg_key = sm.cand_key + warp * kStreamSeg;
+  auto classify = [&](uint32_t key, int i) -> bool {
+    const uint32_t pre = key >> 20;
+    if (kFirst) {
+      atomicAdd(&sm.hist[pre], 1u);
+      return pre >= bin;
+    }
+    if (pre > bin) atomicOr(&sm.sel[i >> 5], 1u << (i & 31));
+    return pre == bin;
+  };
+  auto append = [&](uint32_t& slot, uint32_t key, int i) {
+    if (slot < (uint32_t)kStreamSeg) {
+      seg_idx[slot] = (uint32_t)i;
+      seg_key[slot] = key;
+    }
+    ++slot;
+  };
+  if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0u) {
+    const int n4 = L >> 2;
+    const uint4* p4 = reinterpret_cast<const uint4*>(p);
+    for (int base = 0; base < n4; base += kStreamVec * kStreamThreads) {
+      uint4 key[kStreamVec];   // raw score bits, turned into keys in place
+#pragma unroll
+      for (int u = 0; u < kStreamVec; ++u) {
+        const int i = base + u * kStreamThreads + tid;
+        if (i < n4) key[u] = p4[i];
+      }
+      uint32_t m = 0u;
+#pragma unroll
+      for (int u = 0; u < kStreamVec; ++u) {
         const int i = base + u * kStreamThreads + tid;
         if (i < n4) {
-          const uint32_t k0 = score_key(v[u].x), k1 = score_key(v[u].y);
-          const uint32_t k2 = score_key(v[u].z), k3 = score_key(v[u].w);
-          reinterpret_cast<uint2*>(pre)[i] =
-              make_uint2((k0 >> 16) | (k1 & 0xFFFF0000u), (k2 >> 16) | (k3 & 0xFFFF0000u));
-          atomicAdd(&hist[k0 >> 20], 1u);
-          atomicAdd(&hist[k1 >> 20], 1u);
-          atomicAdd(&hist[k2 >> 20], 1u);
-          atomicAdd(&hist[k3 >> 20], 1u);
+          key[u].x = score_key(__uint_as_float(key[u].x));
+          key[u].y = score_key(__uint_as_float(key[u].y));
+          key[u].z = score_key(__uint_as_float(key[u].z));
+          key[u].w = score_key(__uint_as_float(key[u].w));
+          m |= (classify(key[u].x, 4 * i) ? 1u : 0u) << (4 * u);
+          m |= (classify(key[u].y, 4 * i + 1) ? 2u : 0u) << (4 * u);
+          m |= (classify(key[u].z, 4 * i + 2) ? 4u : 0u) << (4 * u);
+          m |= (classify(key[u].w, 4 * i + 3) ? 8u : 0u) << (4 * u);
+        }
+      }
+      uint32_t slot = stream_reserve(__popc(m), used);
+      if (m) {
+#pragma unroll
+        for (int u = 0; u < kStreamVec; ++u) {
+          const int i = base + u * kStreamThreads + tid;
+          if ((m >> (4 * u)) & 1u) append(slot, key[u].x, 4 * i);
+          if ((m >> (4 * u)) & 2u) append(slot, key[u].y, 4 * i + 1);
+          if ((m >> (4 * u)) & 4u) append(slot, key[u].z, 4 * i + 2);
+          if ((m >> (4 * u)) & 8u) append(slot, key[u].w, 4 * i + 3);
         }
       }
     }
-    for (int i = (n4 << 2) + tid; i < L; i += kStreamThreads) {
-      const uint32_t kk = score_key(p[i]);
-      pre[i] = (uint16_t)(kk >> 16);
-      atomicAdd(&hist[kk >> 20], 1u);
+    // The last L % 4 keys (fewer than 4, all in warp 0).
+    if (warp == 0) {
+      const int i = (n4 << 2) + tid;
+      uint32_t key = 0u;
+      bool hit = false;
+      if (i < L) {
+        key = score_key(p[i]);
+        hit = classify(key, i);
+      }
+      uint32_t slot = stream_reserve(hit ? 1u : 0u, used);
+      if (hit) append(slot, key, i);
     }
   } else {
-    for (int base = 0; base < L; base += 8 * kStreamThreads) {
-      float v[8];
+    for (int base = 0; base < L; base += kStreamVec * kStreamThreads) {
+      uint32_t key[kStreamVec];   // raw score bits, turned into keys in place
+      const uint32_t* pb = reinterpret_cast<const uint32_t*>(p);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kStreamVec; ++u) {
         const int i = base + u * kStreamThreads + tid;
-        if (i < L) v[u] = p[i];
+        if (i < L) key[u] = pb[i];
       }
+      uint32_t m = 0u;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kStreamVec; ++u) {
         const int i = base + u * kStreamThreads + tid;
         if (i < L) {
-          const uint32_t kk = score_key(v[u]);
-          pre[i] = (uint16_t)(kk >> 16);
-          atomicAdd(&hist[kk >> 20], 1u);
+          key[u] = score_key(__uint_as_float(key[u]));
+          m |= (classify(key[u], i) ? 1u : 0u) << u;
         }
+      }
+      uint32_t slot = stream_reserve(__popc(m), used);
+      if (m) {
+#pragma unroll
+        for (int u = 0; u < kStreamVec; ++u)
+          if ((m >> u) & 1u) append(slot, key[u], base + u * kStreamThreads + tid);
       }
     }
   }
-  __syncthreads();
+  if ((tid & 31) == 0) {
+    sm.nseg[warp] = used;
+    if (used > (uint32_t)kStreamSeg) sm.overflow = 1u;
+  }
+}
 
-  // Threshold: prefix P of the key at `shift` resolved bits, `take` of the
-  // keys equal to it are selected (the lowest positions).
-  uint32_t take = (uint32_t)k, P, cnt, b;
-  int shift = 20;
-  stream_pick(hist, kStreamBins, take, scan_buf, pick, P, cnt, take);
-  if (cnt != take) {
-    // Pass B (shared memory only): next 4 bits among keys with prefix P.
-    if (tid < 16) hist[tid] = 0u;
-    __syncthreads();
-    for (int i = tid; i < L; i += kStreamThreads) {
-      const uint32_t v = pre[i];
-      if ((v >> 4) == P) atomicAdd(&hist[v & 15u], 1u);
+__global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_kernel(
+    const float* __restrict__ scores, int64_t stride, int64_t rows,
+    const int32_t* __restrict__ starts, const int32_t* __restrict__ ends, int k,
+    int32_t* __restrict__ out) {
+  extern __shared__ __align__(16) unsigned char stream_smem_raw[];
+  StreamSmem& sm = *reinterpret_cast<StreamSmem*>(stream_smem_raw);
+  const int tid = threadIdx.x;
+  uint32_t guess = kStreamNoGuess;
+
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    __syncthreads();   // the previous row's shared state is no longer read
+    int64_t s;
+    const int L = stream_row_len(starts, ends, row, stride, s);
+    int32_t* __restrict__ orow = out + row * (int64_t)k;
+    if (L <= k) {   // every position is selected; no score is read
+      for (int j = tid; j < k; j += kStreamThreads) orow[j] = j < L ? j : -1;
+      continue;
     }
+    const float* __restrict__ p = scores + row * stride + s;
+
+    for (int i = tid; i < kStreamBins; i += kStreamThreads) sm.hist[i] = 0u;
+    for (int i = tid; i < kStreamWords; i += kStreamThreads) {
+      sm.sel[i] = 0u;
+      sm.eqb[i] = 0u;
+    }
+    if (tid == 0) sm.overflow = 0u;
     __syncthreads();
-    stream_pick(hist, 16, take, scan_buf, pick, b, cnt, take);
-    P = (P << 4) | b;
-    shift = 16;
-    // Passes C and D: low 16 bits, read back for the keys of bucket P only.
-    for (int pass = 0; pass < 2 && cnt != take; ++pass) {
-      const int nshift = shift - 8;
-      if (tid < 256) hist[tid] = 0u;
+
+    stream_pass<true>(p, L, guess, sm);
+    __syncthreads();
+
+    // Threshold state: `P` is the threshold key's prefix with `shift` low
+    // bits dropped; `take` of the keys with that prefix (the lowest
+    // positions) are selected, out of `cnt`.
+    uint32_t take = (uint32_t)k, P, cnt, b;
+    stream_pick(sm.hist, kStreamBins, take, sm, P, cnt, take);
+    const uint32_t P12 = P;
+    const bool first_list_ok = guess <= P12 && sm.overflow == 0u;
+    guess = P12 > 0u ? P12 - 1u : 0u;   // for this CTA's next row
+    __syncthreads();
+    if (!first_list_ok) {
+      if (tid == 0) sm.overflow = 0u;
       __syncthreads();
-      for (int i = tid; i < L; i += kStreamThreads) {
-        if ((uint32_t)pre[i] == (P >> (16 - shift))) {
-          const uint32_t kk = score_key(p[i]);
-          if ((kk >> shift) == P) atomicAdd(&hist[(kk >> nshift) & 255u], 1u);
+      stream_pass<false>(p, L, P12, sm);
+      __syncthreads();
+    }
+    // Each warp walks its own list segment.
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t nc = sm.nseg[warp];
+    const uint32_t* const seg_idx = sm.cand_idx + warp * kStreamSeg;
+    const uint32_t* const seg_key = sm.cand_key + warp * kStreamSeg;
+    const bool list_ok = sm.overflow == 0u;
+    if (first_list_ok) {
+      // The list also holds keys above bin P12 and some below it.
+      for (uint32_t c = lane; c < nc; c += 32) {
+        const uint32_t idx = seg_idx[c];
+        if ((seg_key[c] >> 20) > P12) atomicOr(&sm.sel[idx >> 5], 1u << (idx & 31u));
+      }
+    }
+
+    // Resolve the low 20 bits among keys of bin P12: 8, 8, then 4 bits.
+    int shift = 20;
+    for (int pass = 0; pass < 3 && cnt != take; ++pass) {
+      const int width = pass < 2 ? 8 : 4;
+      const int nshift = shift - width;
+      const uint32_t dmask = (1u << width) - 1u;
+      if (tid < 256) sm.hsmall[tid] = 0u;
+      __syncthreads();
+      if (list_ok) {
+        for (uint32_t c = lane; c < nc; c += 32) {
+          const uint32_t key = seg_key[c];
+          if ((key >> shift) == P) atomicAdd(&sm.hsmall[(key >> nshift) & dmask], 1u);
+        }
+      } else {
+        for (int i = tid; i < L; i += kStreamThreads) {
+          const uint32_t key = score_key(p[i]);
+          if ((key >> shift) == P) atomicAdd(&sm.hsmall[(key >> nshift) & dmask], 1u);
         }
       }
       __syncthreads();
-      stream_pick(hist, 256, take, scan_buf, pick, b, cnt, take);
-      P = (P << 8) | b;
+      stream_pick(sm.hsmall, 1 << width, take, sm, b, cnt, take);
+      P = (P << width) | b;
       shift = nshift;
     }
-  }
 
-  // Ordered compaction: warp w owns the contiguous segment [w*seg, w*seg+seg).
-  const uint32_t p16 = P >> (shift >= 16 ? 0 : 16 - shift);   // bucket at 16 bits
-  auto classify = [&](int i, bool& gt, bool& eq) {
-    const uint32_t v = pre[i];
-    if (shift >= 16) {
-      const uint32_t hi = v >> (shift - 16);
-      gt = hi > P;
-      eq = hi == P;
-    } else if (v != p16) {
-      gt = v > p16;
-      eq = false;
+    // Mark the selected keys of bin P12; keys tied at the threshold go to
+    // `eqb` when only some of them are selected.
+    auto mark = [&](uint32_t key, uint32_t idx) {
+      if ((key >> 20) != P12) return;
+      const uint32_t hi = key >> shift;
+      if (hi > P || (hi == P && cnt == take))
+        atomicOr(&sm.sel[idx >> 5], 1u << (idx & 31u));
+      else if (hi == P)
+        atomicOr(&sm.eqb[idx >> 5], 1u << (idx & 31u));
+    };
+    if (list_ok) {
+      for (uint32_t c = lane; c < nc; c += 32) mark(seg_key[c], seg_idx[c]);
     } else {
-      const uint32_t hi = score_key(p[i]) >> shift;
-      gt = hi > P;
-      eq = hi == P;
+      for (int i = tid; i < L; i += kStreamThreads) mark(score_key(p[i]), (uint32_t)i);
     }
-  };
-  const int seg = ((L + kStreamWarps - 1) / kStreamWarps + 31) & ~31;
-  const int w0 = warp * seg;
-  const int w1 = min(L, w0 + seg);
-  uint32_t ngt = 0u, neq = 0u;
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    bool gt = false, eq = false;
-    if (i < w1) classify(i, gt, eq);
-    ngt += __popc(__ballot_sync(0xffffffffu, gt));
-    neq += __popc(__ballot_sync(0xffffffffu, eq));
-  }
-  if (lane == 0) {
-    wcount[warp][0] = ngt;
-    wcount[warp][1] = neq;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t cg = wcount[lane][0], ce = wcount[lane][1];
-    const uint32_t og = cg, oe = ce;
+    __syncthreads();
+
+    // Thread t owns bitmap words [4t, 4t + 4): positions [128t, 128t + 128).
+    uint32_t w[kStreamWordsPerThread];
+    uint32_t n = 0u;
+    if (cnt != take) {
+      // Keys equal at all 32 bits: the lowest `take` positions win.
+      uint32_t e[kStreamWordsPerThread];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t yg = __shfl_up_sync(0xffffffffu, cg, o);
-      const uint32_t ye = __shfl_up_sync(0xffffffffu, ce, o);
-      if (lane >= o) {
-        cg += yg;
-        ce += ye;
+      for (int q = 0; q < kStreamWordsPerThread; ++q) {
+        e[q] = sm.eqb[kStreamWordsPerThread * tid + q];
+        n += __popc(e[q]);
+      }
+      uint32_t tot;
+      uint32_t r = block_exclusive_scan_nt<kStreamThreads>(n, sm.scan_buf, tot);
+      n = 0u;
+#pragma unroll
+      for (int q = 0; q < kStreamWordsPerThread; ++q) {
+        w[q] = sm.sel[kStreamWordsPerThread * tid + q];
+        if (r < take) w[q] |= first_set_bits(e[q], take - r);
+        r += __popc(e[q]);
+        n += __popc(w[q]);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kStreamWordsPerThread; ++q) {
+        w[q] = sm.sel[kStreamWordsPerThread * tid + q];
+        n += __popc(w[q]);
       }
     }
-    wcount[lane][0] = cg - og;   // exclusive
-    wcount[lane][1] = ce - oe;
-  }
-  __syncthreads();
-  uint32_t g = wcount[warp][0];
-  uint32_t qe = wcount[warp][1];
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    bool gt = false, eq = false;
-    if (i < w1) classify(i, gt, eq);
-    const uint32_t bg = __ballot_sync(0xffffffffu, gt);
-    const uint32_t be = __ballot_sync(0xffffffffu, eq);
-    const uint32_t my_g = g + __popc(bg & lt_mask);
-    const uint32_t my_e = qe + __popc(be & lt_mask);
-    if (gt) orow[my_g + min(my_e, take)] = i;
-    else if (eq && my_e < take) orow[my_g + my_e] = i;
-    g += __popc(bg);
-    qe += __popc(be);
+    uint32_t total;
+    uint32_t pos = block_exclusive_scan_nt<kStreamThreads>(n, sm.scan_buf, total);
+#pragma unroll
+    for (int q = 0; q < kStreamWordsPerThread; ++q) {
+      uint32_t bits = w[q];
+      const int base = 32 * (kStreamWordsPerThread * tid + q);
+      while (bits) {
+        const int e = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        if (pos < (uint32_t)k) orow[pos] = base + e;
+        ++pos;
+      }
+    }
   }
 }
 
@@ -774,18 +1132,36 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
   // (or longer ones): a cluster per row, so that one row's work is spread
   // over several SMs. The selected set is unique, so the kernel choice never
   // changes the output.
+  if (stride <= kRowMaxLen) {
+    static std::atomic<bool> row_attr{false};
+    if (!row_attr.load(std::memory_order_acquire)) {
+      cudaError_t e = cudaFuncSetAttribute(topk_smem_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)sizeof(RowSmem));
+      if (e != cudaSuccess) return e;
+      row_attr.store(true, std::memory_order_release);
+    }
+    topk_smem_kernel<<<(unsigned)rows, kRowThreads, sizeof(RowSmem), stream>>>(scores, stride,
+                                                                              starts, ends, k, out);
+    return cudaGetLastError();
+  }
   if (stride <= kStreamMaxLen && rows >= kStreamMinRows) {
-    const size_t smem = ((size_t)stride * sizeof(uint16_t) + 15) & ~size_t(15);
     static std::atomic<bool> stream_attr{false};
     if (!stream_attr.load(std::memory_order_acquire)) {
       cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)(kStreamMaxLen * sizeof(uint16_t)));
+                                           (int)sizeof(StreamSmem));
       if (e != cudaSuccess) return e;
       stream_attr.store(true, std::memory_order_release);
     }
-    topk_stream_kernel<<<(unsigned)rows, kStreamThreads, smem, stream>>>(scores, stride, starts,
-                                                                         ends, k, out);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = (int64_t)sms * kStreamCtasPerSm;
+    const int64_t grid = rows < slots ? rows : slots;
+    topk_stream_kernel<<<(unsigned)grid, kStreamThreads, sizeof(StreamSmem), stream>>>(
+        scores, stride, rows, starts, ends, k, out);
     return cudaGetLastError();
   }
   // Cluster size from the row stride alone: about 8K keys per CTA, at most 8

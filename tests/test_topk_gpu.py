@@ -5,7 +5,10 @@ decode batches, sampled rows of the chunked-prefill score matrix), and the
 edge cases of "Deterministic sparse top-k" (PR 54955) and "What is fixed"
 (PR 51538): heavy ties, signed zeros, NaN and -inf, negative and oversized
 lengths, offsets that break 16-byte alignment, rows shorter than, equal to
-and one longer than k, and empty batches.
+and one longer than k, and empty batches. Row widths and batch sizes are
+chosen so that every kernel behind ds_topk_per_row runs: whole rows in
+shared memory (width <= 32768), the streaming grid (>= 256 rows of up to
+65536), and a cluster per row (otherwise).
 """
 
 import numpy as np
@@ -201,9 +204,11 @@ def _mixed_rows(rng, R, stride, k):
     return s, starts, ends
 
 
-@pytest.mark.parametrize("stride,k", [(20000, 2048), (20001, 700), (9000, 64)])
+@pytest.mark.parametrize("stride,k", [(20000, 2048), (20001, 700), (9000, 64), (32768, 2048),
+                                      (40001, 2048), (50000, 700)])
 def test_many_rows_mixed_cases_exact(ds, stride, k):
-    # At least 256 rows of at most 64K scores: one CTA per row streams the row.
+    # Rows of up to 32K scores are held whole in shared memory; batches of at
+    # least 256 longer rows (up to 64K) are streamed by a persistent grid.
     rng = np.random.default_rng(stride + k)
     s, a, b = _mixed_rows(rng, 288, stride, k)
     check(ds, s, a, b, k)
@@ -219,12 +224,17 @@ def test_many_rows_longest_rows_sampled(ds):
     assert np.array_equal(got[rows], want)
 
 
-def test_stream_and_cluster_kernels_agree(ds):
-    # The same rows alone (a cluster per row) and inside a batch of 300 rows
-    # (one streaming CTA per row) give identical indices.
+def test_kernel_choice_never_changes_indices(ds):
+    # The same rows alone in a 40000-wide matrix (a cluster per row), in a
+    # batch of 300 such rows (the streaming kernel) and in a 30000-wide
+    # matrix (whole row in shared memory) give identical indices.
     rng = np.random.default_rng(12)
     s, a, b = _mixed_rows(rng, 300, 30000, 2048)
-    big = run(ds, s, a, b, 2048)
+    wide = np.full((300, 40000), np.nan, np.float32)
+    wide[:, :30000] = s
+    narrow = run(ds, s, a, b, 2048)
+    big = run(ds, wide, a, b, 2048)
+    assert np.array_equal(big, narrow)
     for r in [0, 1, 3, 4, 5, 7, 8, 299]:
-        one = run(ds, s[r:r + 1], a[r:r + 1], b[r:r + 1], 2048)[0]
+        one = run(ds, wide[r:r + 1], a[r:r + 1], b[r:r + 1], 2048)[0]
         assert np.array_equal(one, big[r]), r
