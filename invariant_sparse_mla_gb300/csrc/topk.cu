@@ -531,27 +531,28 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
 // Rows of up to 32768 scores: one 1024-thread CTA per row, the whole row in
 // shared memory. Every thread issues asynchronous 16-byte copies for its
 // share of the row (4-byte copies when the row start is not 16-byte
-// aligned), so the full row is in flight at once without holding registers.
-// The keys are formed in place while the 12-bit histogram is built; the low
-// 20 bits of the threshold are resolved by 8-, 8- and 4-bit histogram passes
-// over shared memory that count only keys still tied with the threshold
-// prefix. One more pass writes the selection as a bitmap (eight lanes share a
-// 32-position word), ties at the full key go to the lowest positions by a
-// prefix count over the tied-key bitmap, and thread t turns bitmap word t
-// into output slots after one block-wide scan.
+// aligned) in four commit groups, and turns each group into keys and
+// 12-bit histogram counts as soon as its own copies have landed.
+//
+// After the threshold bin is picked, one pass gives every thread the
+// selection word of its own 32 positions: keys above the bin are selected,
+// keys in the bin are marked as tied. The bin's low 20 bits are resolved by
+// 8-, 8- and 4-bit histogram passes that visit only the tied positions, and
+// each thread then settles its own tied keys. Keys equal to the threshold
+// at all 32 bits go to the lowest positions by one block-wide scan of the
+// tied counts, and a last scan of the selected counts gives every output
+// slot in index order. Apart from the histograms, no step uses atomics.
 
 constexpr int kRowThreads = 1024;
 constexpr int kRowMaxLen = 32768;
-constexpr int kRowWords = kRowMaxLen / 32;   // one per thread
 constexpr int kRowBins = 4096;
+constexpr int kRowGroups = 4;   // commit groups of the row copy
 
 struct RowSmem {
   uint32_t key[kRowMaxLen];
   uint32_t hist[kRowBins];
-  uint32_t sel[kRowWords];
-  uint32_t eqb[kRowWords];
-  uint32_t hsmall[256];
-  uint32_t scan_buf[32];
+  uint32_t hsmall[3][256];   // one per refinement pass, zeroed up front
+  uint32_t wsum[32];
   uint32_t pick[3];
 };
 
@@ -567,32 +568,50 @@ __device__ __forceinline__ void cp_async_4B(void* dst, const void* src) {
                "l"(src)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+__device__ __forceinline__ void cp_async_commit_group() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Picks, among `nbins` bins counted in `hist` (descending bin order), the bin
+// Picks, among NBINS bins counted in `hist` (descending bin order), the bin
 // holding the `take`-th largest key: every thread gets (bin, count of that
-// bin, take within that bin). Bins per thread: ceil(4096 / NT).
-template <int NT>
-__device__ __forceinline__ void block_pick(const uint32_t* hist, int nbins, uint32_t take,
-                                           uint32_t* scan_buf, uint32_t* pick, uint32_t& bin,
-                                           uint32_t& cnt, uint32_t& take_in_bin) {
-  constexpr int kPer = (4096 + NT - 1) / NT;
-  const int tid = threadIdx.x;
+// bin, take within that bin). Two block barriers.
+template <int NBINS>
+__device__ __forceinline__ void row_pick(const uint32_t* hist, uint32_t take, uint32_t* wsum,
+                                         uint32_t* pick, uint32_t& bin, uint32_t& cnt,
+                                         uint32_t& take_in_bin) {
+  constexpr int kPer = NBINS >= kRowThreads ? NBINS / kRowThreads : 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t c[kPer];
   uint32_t mine = 0u;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    const int b = nbins - 1 - (tid * kPer + q);
+    const int b = NBINS - 1 - (tid * kPer + q);
     c[q] = b >= 0 ? hist[b] : 0u;
     mine += c[q];
   }
-  uint32_t total;
-  uint32_t above = block_exclusive_scan_nt<NT>(mine, scan_buf, total);
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  const uint32_t ws = wsum[lane];
+  uint32_t wincl = ws;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += y;
+  }
+  uint32_t above = __shfl_sync(0xffffffffu, wincl - ws, warp) + incl - mine;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    const int b = nbins - 1 - (tid * kPer + q);
+    const int b = NBINS - 1 - (tid * kPer + q);
     if (b >= 0 && above < take && take <= above + c[q]) {
       pick[0] = (uint32_t)b;
       pick[1] = take - above;
@@ -604,7 +623,6 @@ __device__ __forceinline__ void block_pick(const uint32_t* hist, int nbins, uint
   bin = pick[0];
   take_in_bin = pick[1];
   cnt = pick[2];
-  __syncthreads();
 }
 
 // Mask of the first m set bits of x.
@@ -616,6 +634,11 @@ __device__ __forceinline__ uint32_t first_set_bits(uint32_t x, uint32_t m) {
     x ^= low;
   }
   return r;
+}
+
+__device__ __forceinline__ uint4 keys_of(uint4 w) {
+  return make_uint4(score_key(__uint_as_float(w.x)), score_key(__uint_as_float(w.y)),
+                    score_key(__uint_as_float(w.z)), score_key(__uint_as_float(w.w)));
 }
 
 __global__ void __launch_bounds__(kRowThreads, 1) topk_smem_kernel(
@@ -641,113 +664,139 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_smem_kernel(
   }
   const float* __restrict__ p = scores + row * stride + s;
 
-  // The whole row in flight. Key slot i holds position i; slots from L up to
-  // the next multiple of 4 hold bytes of the same 16-byte granules and are
-  // never counted or selected.
+  // Key slot i holds position i. Thread t copies granules (4 slots) t,
+  // t + 1024, ...; group g holds its granules 2g and 2g + 1. Slots from L
+  // up to the next multiple of 4 hold bytes of the row's last 16-byte
+  // granule and are never counted or selected.
   const int n4 = (L + 3) >> 2;
-  if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0u) {
-    for (int j = tid; j < n4; j += kRowThreads) cp_async_16B(&sm.key[4 * j], p + 4 * j);
-  } else {
-    for (int i = tid; i < L; i += kRowThreads) cp_async_4B(&sm.key[i], p + i);
+  const bool aligned = (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
+#pragma unroll
+  for (int g = 0; g < kRowGroups; ++g) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = (2 * g + h) * kRowThreads + tid;
+      if (j < n4) {
+        if (aligned) {
+          cp_async_16B(&sm.key[4 * j], p + 4 * j);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (4 * j + q < L) cp_async_4B(&sm.key[4 * j + q], p + 4 * j + q);
+        }
+      }
+    }
+    cp_async_commit_group();
   }
   for (int i = tid; i < kRowBins; i += kRowThreads) sm.hist[i] = 0u;
-  sm.sel[tid] = 0u;
-  sm.eqb[tid] = 0u;
-  cp_async_commit_wait_all();
-  __syncthreads();
+  for (int i = tid; i < 3 * 256; i += kRowThreads) (&sm.hsmall[0][0])[i] = 0u;
+  __syncthreads();   // histograms zeroed
 
-  // Keys in place, and the histogram of their top 12 bits.
+  // Keys in place, and the histogram of their top 12 bits, group by group.
   uint4* const key4 = reinterpret_cast<uint4*>(sm.key);
-  for (int j = tid; j < n4; j += kRowThreads) {
-    uint4 w = key4[j];
-    w.x = score_key(__uint_as_float(w.x));
-    w.y = score_key(__uint_as_float(w.y));
-    w.z = score_key(__uint_as_float(w.z));
-    w.w = score_key(__uint_as_float(w.w));
-    key4[j] = w;
-    const int valid = min(4, L - 4 * j);
-    atomicAdd(&sm.hist[w.x >> 20], 1u);
-    if (valid > 1) atomicAdd(&sm.hist[w.y >> 20], 1u);
-    if (valid > 2) atomicAdd(&sm.hist[w.z >> 20], 1u);
-    if (valid > 3) atomicAdd(&sm.hist[w.w >> 20], 1u);
-  }
+  auto convert = [&](int g) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = (2 * g + h) * kRowThreads + tid;
+      if (j < n4) {
+        const uint4 w = keys_of(key4[j]);
+        key4[j] = w;
+        if (4 * j + 4 <= L) {
+          atomicAdd(&sm.hist[w.x >> 20], 1u);
+          atomicAdd(&sm.hist[w.y >> 20], 1u);
+          atomicAdd(&sm.hist[w.z >> 20], 1u);
+          atomicAdd(&sm.hist[w.w >> 20], 1u);
+        } else {
+          atomicAdd(&sm.hist[w.x >> 20], 1u);
+          if (4 * j + 1 < L) atomicAdd(&sm.hist[w.y >> 20], 1u);
+          if (4 * j + 2 < L) atomicAdd(&sm.hist[w.z >> 20], 1u);
+        }
+      }
+    }
+  };
+  cp_async_wait_group<3>();
+  convert(0);
+  cp_async_wait_group<2>();
+  convert(1);
+  cp_async_wait_group<1>();
+  convert(2);
+  cp_async_wait_group<0>();
+  convert(3);
   __syncthreads();
 
   // Threshold state: `P` is the threshold key's prefix with `shift` low bits
   // dropped; `take` of the `cnt` keys with that prefix (the lowest positions)
   // are selected.
   uint32_t take = (uint32_t)k, P, cnt, b;
-  block_pick<kRowThreads>(sm.hist, kRowBins, take, sm.scan_buf, sm.pick, P, cnt, take);
+  row_pick<kRowBins>(sm.hist, take, sm.wsum, sm.pick, P, cnt, take);
+
+  // Thread t's positions [32t, 32t + 32): 8 granules, read in a lane-rotated
+  // order so that the warp's 16-byte reads hit distinct banks.
+  const int base = 32 * tid;
+  uint32_t sel = 0u, eqw = 0u;
+  if (base < L) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int cc = (c + lane) & 7;
+      const uint4 w = key4[8 * tid + cc];
+      const uint32_t kk[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t pre = kk[q] >> 20;
+        sel |= (pre > P ? 1u : 0u) << (4 * cc + q);
+        eqw |= (pre == P ? 1u : 0u) << (4 * cc + q);
+      }
+    }
+    if (L - base < 32) {
+      const uint32_t valid = (1u << (L - base)) - 1u;
+      sel &= valid;
+      eqw &= valid;
+    }
+  }
+
   int shift = 20;
   for (int pass = 0; pass < 3 && cnt != take; ++pass) {
     const int width = pass < 2 ? 8 : 4;
     const int nshift = shift - width;
     const uint32_t dmask = (1u << width) - 1u;
-    if (tid < 256) sm.hsmall[tid] = 0u;
-    __syncthreads();
-    for (int j = tid; j < n4; j += kRowThreads) {
-      const uint4 w = key4[j];
-      const int valid = min(4, L - 4 * j);
-      if ((w.x >> shift) == P) atomicAdd(&sm.hsmall[(w.x >> nshift) & dmask], 1u);
-      if (valid > 1 && (w.y >> shift) == P) atomicAdd(&sm.hsmall[(w.y >> nshift) & dmask], 1u);
-      if (valid > 2 && (w.z >> shift) == P) atomicAdd(&sm.hsmall[(w.z >> nshift) & dmask], 1u);
-      if (valid > 3 && (w.w >> shift) == P) atomicAdd(&sm.hsmall[(w.w >> nshift) & dmask], 1u);
+    uint32_t* const hs = sm.hsmall[pass];
+    for (uint32_t m = eqw; m; m &= m - 1u) {
+      const uint32_t key = sm.key[base + __ffs(m) - 1];
+      if ((key >> shift) == P) atomicAdd(&hs[(key >> nshift) & dmask], 1u);
     }
     __syncthreads();
-    block_pick<kRowThreads>(sm.hsmall, 1 << width, take, sm.scan_buf, sm.pick, b, cnt, take);
+    if (width == 8) row_pick<256>(hs, take, sm.wsum, sm.pick, b, cnt, take);
+    else row_pick<16>(hs, take, sm.wsum, sm.pick, b, cnt, take);
     P = (P << width) | b;
     shift = nshift;
   }
 
-  // Selection bitmap: lanes 8m..8m+7 of a warp hold the 32 positions of one
-  // word; their nibbles are OR-ed together and lane 8m stores the word.
+  // Settle this thread's tied keys: above the threshold, or tied with it.
   const bool all_eq = cnt == take;
-  for (int j0 = 0; j0 < n4; j0 += kRowThreads) {
-    const int j = j0 + tid;
-    uint32_t gt = 0u, eq = 0u;
-    if (j < n4) {
-      const uint4 w = key4[j];
-      const uint32_t kk[4] = {w.x, w.y, w.z, w.w};
-      const int valid = min(4, L - 4 * j);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t hi = kk[q] >> shift;
-        if (q < valid) {
-          gt |= (hi > P || (all_eq && hi == P) ? 1u : 0u) << q;
-          eq |= (!all_eq && hi == P ? 1u : 0u) << q;
-        }
-      }
+  if (shift < 20) {
+    uint32_t tied = 0u;
+    for (uint32_t m = eqw; m; m &= m - 1u) {
+      const int bit = __ffs(m) - 1;
+      const uint32_t hi = sm.key[base + bit] >> shift;
+      if (hi > P) sel |= 1u << bit;
+      else if (hi == P) tied |= 1u << bit;
     }
-    const int sh = 4 * (lane & 7);
-    gt <<= sh;
-    eq <<= sh;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      gt |= __shfl_xor_sync(0xffffffffu, gt, o);
-      eq |= __shfl_xor_sync(0xffffffffu, eq, o);
-    }
-    if ((lane & 7) == 0 && j < n4) {
-      sm.sel[j >> 3] = gt;
-      sm.eqb[j >> 3] = eq;
-    }
+    eqw = tied;
   }
-  __syncthreads();
-
-  // Thread t owns word t: positions [32t, 32t + 32).
-  uint32_t w = sm.sel[tid];
-  if (!all_eq) {
+  if (all_eq) {
+    sel |= eqw;
+  } else {
     // Keys equal at all 32 bits: the lowest `take` positions win.
-    const uint32_t eqw = sm.eqb[tid];
     uint32_t tot;
-    const uint32_t r = block_exclusive_scan_nt<kRowThreads>(__popc(eqw), sm.scan_buf, tot);
-    if (r < take) w |= first_set_bits(eqw, take - r);
+    const uint32_t r =
+        block_exclusive_scan_nt<kRowThreads>(__popc(eqw), sm.wsum, tot);
+    if (r < take) sel |= first_set_bits(eqw, take - r);
   }
   uint32_t total;
-  uint32_t pos = block_exclusive_scan_nt<kRowThreads>(__popc(w), sm.scan_buf, total);
-  while (w) {
-    const int bit = __ffs(w) - 1;
-    w &= w - 1u;
-    if (pos < (uint32_t)k) orow[pos] = 32 * tid + bit;
+  uint32_t pos = block_exclusive_scan_nt<kRowThreads>(__popc(sel), sm.wsum, total);
+  while (sel) {
+    const int bit = __ffs(sel) - 1;
+    sel &= sel - 1u;
+    if (pos < (uint32_t)k) orow[pos] = base + bit;
     ++pos;
   }
 }
