@@ -261,23 +261,26 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       pos[i] = t < ntiles ? idx_row[j0 + t * kTile + pw * 16 + (lane & 15)] : -1;
       if (pos[i] != -1) last = t + 1;
     }
+    // All four block-table reads go out before any is used: one round trip.
+    int64_t page[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ps = pos[i];
+      page[i] = -2;   // no lookup
+      if (ps >= 0 && (int64_t)ps < len && row_ok && (int64_t)(ps >> 6) < p.bt_stride)
+        page[i] = p.block_table[bt_row * p.bt_stride + (ps >> 6)];
+    }
     int err_bits = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int ps = pos[i];
       bool valid = false;
       if (ps >= 0 && (int64_t)ps < len && row_ok) {
-        const int64_t blk = ps >> 6;
-        if (blk < p.bt_stride) {
-          const int64_t page = p.block_table[bt_row * p.bt_stride + blk];
-          if (page >= 0 && page < p.num_pages) {
-            grow[i] = (int)(page * 64 + (ps & 63));
-            valid = true;
-          } else {
-            err_bits |= kErrPage;
-          }
+        if (page[i] >= 0 && page[i] < p.num_pages) {
+          grow[i] = (int)(page[i] * 64 + (ps & 63));
+          valid = true;
         } else {
-          err_bits |= kErrPage;
+          err_bits |= kErrPage;   // outside the pool, or beyond the block table
         }
       } else if (ps != -1 && row_ok) {
         err_bits |= kErrIdx;
