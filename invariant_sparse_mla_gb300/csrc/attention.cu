@@ -179,6 +179,8 @@ struct KParams {
 
 template <int HG, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KParams p) {
+  pdl_wait();
+  pdl_trigger();
   using LY = Layout<HG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -648,6 +650,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       int64_t R, int H, int S,
                                                       __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t rh = blockIdx.x;  // row * H + h
   const int t = threadIdx.x;
   const int64_t RH = R * H;
@@ -704,8 +708,7 @@ cudaError_t launch_split(const KParams& kp, int64_t blocks, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     attr_set.store(true, std::memory_order_release);
   }
-  kern<<<(unsigned)blocks, kThreads, LY::kSmemBytes, stream>>>(kp);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), LY::kSmemBytes, stream, 1u, kp);
 }
 
 }  // namespace
@@ -764,10 +767,9 @@ cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream) {
   else
     e = fp8 ? launch_split<16, true>(kp, blocks, stream) : launch_split<16, false>(kp, blocks, stream);
   if (e != cudaSuccess) return e;
-  combine_kernel<<<(unsigned)(a.R * a.H), 128, 0, stream>>>(
-      ws.part_o, ws.part_m, ws.part_l, a.R, a.H, kp.num_splits,
-      reinterpret_cast<__nv_bfloat16*>(a.out), a.lse);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)(a.R * a.H)), dim3(128), 0, stream, 1u,
+                    (const float*)ws.part_o, (const float*)ws.part_m, (const float*)ws.part_l, a.R,
+                    a.H, kp.num_splits, reinterpret_cast<__nv_bfloat16*>(a.out), a.lse);
 }
 
 }  // namespace dsmla

@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace dsmla {
 
 // Entries per attention tile and tiles per split. The split count of a call
@@ -50,6 +52,47 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
                         const int32_t* ends, int k, int32_t* out, cudaStream_t stream);
 
 cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream);
+
+// ---- programmatic dependent launch. Every kernel of this library is
+// launched with the programmatic-stream-serialization attribute, so it may
+// become resident while the previous kernel of the stream is still running.
+// It calls pdl_wait() before its first global-memory access (that returns
+// once the previous grid has finished and its writes are visible) and
+// pdl_trigger() to let the next kernel of the stream start the same way.
+// Neither changes what any kernel computes.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// cudaLaunchKernelEx with programmatic stream serialization and, when
+// cluster_x > 1, a (cluster_x, 1, 1) thread-block cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#endif
 
 // Records a printf-style message for ds_last_error() on this host thread and
 // returns `status`.

@@ -113,6 +113,8 @@ __device__ __forceinline__ void load4_keys(const float* __restrict__ p, int64_t 
 __global__ void __launch_bounds__(kThreads) topk_rows_kernel(
     const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ starts,
     const int32_t* __restrict__ ends, int k, int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t scan_buf[32];
   __shared__ uint32_t pick[3];
@@ -286,6 +288,8 @@ __device__ __forceinline__ uint32_t cluster_size() {
 __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
     const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ starts,
     const int32_t* __restrict__ ends, int k, int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint32_t keys[];  // this CTA's chunk
   __shared__ __align__(16) uint32_t hist[2][kBins];
   __shared__ uint32_t scan_buf[32];
@@ -644,6 +648,8 @@ __device__ __forceinline__ uint4 keys_of(uint4 w) {
 __global__ void __launch_bounds__(kRowThreads, 1) topk_smem_kernel(
     const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ starts,
     const int32_t* __restrict__ ends, int k, int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char row_smem_raw[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(row_smem_raw);
   const int tid = threadIdx.x, lane = tid & 31;
@@ -1030,6 +1036,8 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
     const float* __restrict__ scores, int64_t stride, int64_t rows,
     const int32_t* __restrict__ starts, const int32_t* __restrict__ ends, int k,
     int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char stream_smem_raw[];
   StreamSmem& sm = *reinterpret_cast<StreamSmem*>(stream_smem_raw);
   const int tid = threadIdx.x;
@@ -1190,9 +1198,8 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
       if (e != cudaSuccess) return e;
       row_attr.store(true, std::memory_order_release);
     }
-    topk_smem_kernel<<<(unsigned)rows, kRowThreads, sizeof(RowSmem), stream>>>(scores, stride,
-                                                                              starts, ends, k, out);
-    return cudaGetLastError();
+    return launch_pdl(topk_smem_kernel, dim3((unsigned)rows), dim3(kRowThreads), sizeof(RowSmem),
+                      stream, 1u, scores, stride, starts, ends, k, out);
   }
   if (stride <= kStreamMaxLen && rows >= kStreamMinRows) {
     static std::atomic<bool> stream_attr{false};
@@ -1209,9 +1216,8 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)sms * kStreamCtasPerSm;
     const int64_t grid = rows < slots ? rows : slots;
-    topk_stream_kernel<<<(unsigned)grid, kStreamThreads, sizeof(StreamSmem), stream>>>(
-        scores, stride, rows, starts, ends, k, out);
-    return cudaGetLastError();
+    return launch_pdl(topk_stream_kernel, dim3((unsigned)grid), dim3(kStreamThreads),
+                      sizeof(StreamSmem), stream, 1u, scores, stride, rows, starts, ends, k, out);
   }
   // Cluster size from the row stride alone: about 8K keys per CTA, at most 8
   // CTAs. Rows longer than 8 x 16K keys take the single-CTA kernel.
@@ -1219,8 +1225,8 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
   if (C > kMaxCluster) C = kMaxCluster;
   const int64_t per = ((stride + C - 1) / C + 3) & ~int64_t(3);
   if (per > kMaxChunk || rows * C > (int64_t)INT32_MAX) {
-    topk_rows_kernel<<<(unsigned)rows, kThreads, 0, stream>>>(scores, stride, starts, ends, k, out);
-    return cudaGetLastError();
+    return launch_pdl(topk_rows_kernel, dim3((unsigned)rows), dim3(kThreads), 0, stream, 1u, scores,
+                      stride, starts, ends, k, out);
   }
   const size_t smem = (size_t)per * sizeof(uint32_t);
   static std::atomic<bool> attr_set{false};
@@ -1231,19 +1237,8 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
     if (e != cudaSuccess) return e;
     attr_set.store(true, std::memory_order_release);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * C), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, stride, starts, ends, k, out);
+  return launch_pdl(topk_cluster_kernel, dim3((unsigned)(rows * C)), dim3(kThreads), smem, stream,
+                    (unsigned)C, scores, stride, starts, ends, k, out);
 }
 
 }  // namespace dsmla
