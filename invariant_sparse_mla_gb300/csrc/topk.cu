@@ -37,7 +37,6 @@ namespace dsmla {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = kThreads * 4;  // elements per block-wide step
 constexpr int kBins = 2048;
 constexpr int kBinsPerThread = kBins / kThreads;
@@ -229,309 +228,6 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(
 
 
 // ---------------------------------------------------------------------------
-// Cluster variant: the row is cut into C contiguous chunks, one per CTA of a
-// thread-block cluster (C <= 8). Each CTA keeps its chunk's keys in shared
-// memory, so the row is read from HBM exactly once. The per-CTA digit
-// histograms are summed through distributed shared memory after a hardware
-// cluster barrier (every CTA of a cluster is co-scheduled, so the barrier
-// cannot wait on a CTA that never runs); every CTA then derives the same
-// threshold. Histograms are double buffered, so one cluster barrier per digit
-// pass suffices. The compaction counts (greater, equal) per warp with
-// ballots, exchanges the per-CTA totals through distributed shared memory to
-// get each chunk's carry-in, and writes the output in ascending order.
-
-constexpr int kMaxChunk = 16384;       // keys per CTA (64 KiB of shared memory)
-constexpr int kMaxCluster = 8;
-
-// Reads of another CTA's shared memory. They are only issued after a cluster
-// barrier that orders the writes, so they need no memory clobber and may be
-// overlapped freely.
-__device__ __forceinline__ uint32_t dsmem_addr(const void* local_ptr, uint32_t rank) {
-  uint32_t remote;
-  asm("mapa.shared::cluster.u32 %0, %1, %2;"
-      : "=r"(remote)
-      : "r"((uint32_t)__cvta_generic_to_shared(local_ptr)), "r"(rank));
-  return remote;
-}
-
-__device__ __forceinline__ uint32_t dsmem_ld(const uint32_t* local_ptr, uint32_t rank) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(dsmem_addr(local_ptr, rank)));
-  return v;
-}
-
-__device__ __forceinline__ uint4 dsmem_ld4(const uint32_t* local_ptr, uint32_t rank) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(dsmem_addr(local_ptr, rank)));
-  return v;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-__global__ void __launch_bounds__(kThreads) topk_cluster_kernel(
-    const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ starts,
-    const int32_t* __restrict__ ends, int k, int32_t* __restrict__ out) {
-  pdl_wait();
-  pdl_trigger();
-  extern __shared__ __align__(16) uint32_t keys[];  // this CTA's chunk
-  __shared__ __align__(16) uint32_t hist[2][kBins];
-  __shared__ uint32_t scan_buf[32];
-  __shared__ uint32_t pick[3];
-  __shared__ uint32_t wcount[kWarps][2];        // per-warp (greater, equal) counts
-  __shared__ uint32_t cta_tot[2];               // this CTA's totals, read by later ranks
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t C = cluster_size();
-  const uint32_t crank = cluster_rank();
-  const int64_t row = blockIdx.x / C;
-  const int64_t s = starts[row];
-  const int64_t e = ends[row];
-  int64_t L = 0;
-  if (s >= 0 && s <= stride) {
-    L = e - s;
-    if (L < 0) L = 0;
-    if (L > stride - s) L = stride - s;
-  }
-  int32_t* __restrict__ orow = out + row * (int64_t)k;
-  if (L <= (int64_t)k) {  // uniform over the cluster: no cluster barrier is used
-    if (crank == 0)
-      for (int j = tid; j < k; j += kThreads) orow[j] = (int64_t)j < L ? j : -1;
-    return;
-  }
-
-  // Chunk of this CTA: [c0, c0 + n), chunks a multiple of 4 elements long.
-  const int64_t per = ((L + C - 1) / C + 3) & ~int64_t(3);
-  const int64_t c0 = per * crank;
-  const int n = (int)(c0 >= L ? 0 : (L - c0 < per ? L - c0 : per));
-  const float* __restrict__ p = scores + row * stride + s + c0;
-  const bool aligned = (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
-
-  for (int i = tid; i < kBins; i += kThreads) {
-    hist[0][i] = 0u;
-    hist[1][i] = 0u;
-  }
-  __syncthreads();
-
-  // Load the chunk (8 x 16 B per thread in flight), store keys, histogram
-  // of the top 11 bits.
-  if (aligned) {
-    const int n4 = n >> 2;
-    const float4* p4 = reinterpret_cast<const float4*>(p);
-    for (int base = 0; base < n4; base += 8 * kThreads) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kThreads + tid;
-        if (i < n4) v[u] = p4[i];
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kThreads + tid;
-        if (i < n4) {
-          uint4 kk;
-          kk.x = score_key(v[u].x);
-          kk.y = score_key(v[u].y);
-          kk.z = score_key(v[u].z);
-          kk.w = score_key(v[u].w);
-          reinterpret_cast<uint4*>(keys)[i] = kk;
-          atomicAdd(&hist[0][kk.x >> 21], 1u);
-          atomicAdd(&hist[0][kk.y >> 21], 1u);
-          atomicAdd(&hist[0][kk.z >> 21], 1u);
-          atomicAdd(&hist[0][kk.w >> 21], 1u);
-        }
-      }
-    }
-    for (int i = (n4 << 2) + tid; i < n; i += kThreads) {
-      const uint32_t kk = score_key(p[i]);
-      keys[i] = kk;
-      atomicAdd(&hist[0][kk >> 21], 1u);
-    }
-  } else {
-    for (int base = 0; base < n; base += 8 * kThreads) {
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kThreads + tid;
-        if (i < n) v[u] = p[i];
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kThreads + tid;
-        if (i < n) {
-          const uint32_t kk = score_key(v[u]);
-          keys[i] = kk;
-          atomicAdd(&hist[0][kk >> 21], 1u);
-        }
-      }
-    }
-  }
-
-  uint32_t prefix = 0u;
-  int shift = 32;
-  uint32_t take = (uint32_t)k;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int width = pass < 2 ? 11 : 10;
-    const int nshift = shift - width;
-    const uint32_t nbins = 1u << width;
-    const int buf = pass & 1;
-    if (pass > 0) {
-      if (pass == 2) {
-        // hist[0] was last read by the other CTAs in pass 0, before the
-        // cluster barrier of pass 1. (hist[1] starts out zeroed.)
-        for (int i = tid; i < kBins; i += kThreads) hist[0][i] = 0u;
-        __syncthreads();
-      }
-      for (int i = tid; i < n; i += kThreads) {
-        const uint32_t kk = keys[i];
-        if ((kk >> shift) == prefix) atomicAdd(&hist[buf][(kk >> nshift) & (nbins - 1u)], 1u);
-      }
-    }
-    __syncthreads();
-    cluster_sync_all();
-
-    // Cluster-wide counts of this thread's bins (descending bin order): the
-    // thread's four bins are contiguous, so one 16-byte remote load per rank.
-    uint32_t c[kBinsPerThread];
-    uint32_t mine = 0u;
-    const int bhi = (int)nbins - 1 - tid * kBinsPerThread;   // highest of the four
-    {
-      uint4 acc = make_uint4(0u, 0u, 0u, 0u);
-      if (bhi >= kBinsPerThread - 1) {
-        uint4 part[kMaxCluster];
-#pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r)
-          if (r < (int)C) part[r] = dsmem_ld4(&hist[buf][bhi - 3], (uint32_t)r);
-#pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r)
-          if (r < (int)C) {
-            acc.x += part[r].x;
-            acc.y += part[r].y;
-            acc.z += part[r].z;
-            acc.w += part[r].w;
-          }
-      }
-      c[0] = acc.w;  // bin bhi
-      c[1] = acc.z;
-      c[2] = acc.y;
-      c[3] = acc.x;  // bin bhi - 3
-      mine = acc.x + acc.y + acc.z + acc.w;
-    }
-    uint32_t total;
-    uint32_t above = block_exclusive_scan(mine, scan_buf, total);
-#pragma unroll
-    for (int q = 0; q < kBinsPerThread; ++q) {
-      const int b = (int)nbins - 1 - (tid * kBinsPerThread + q);
-      if (b >= 0 && above < take && take <= above + c[q]) {
-        pick[0] = (uint32_t)b;
-        pick[1] = take - above;
-        pick[2] = c[q];
-      }
-      above += c[q];
-    }
-    __syncthreads();
-    const uint32_t b = pick[0];
-    const uint32_t cnt = pick[2];
-    take = pick[1];
-    prefix = (pass == 0 ? 0u : (prefix << width)) | b;
-    shift = nshift;
-    if (cnt == take) break;  // same decision in every CTA of the cluster
-  }
-
-  // Ordered compaction. Warp w owns the contiguous segment [w*seg, w*seg+seg)
-  // of the chunk, read 32 keys at a time.
-  const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
-  const int w0 = warp * seg;
-  const int w1 = min(n, w0 + seg);
-  uint32_t ngt = 0u, neq = 0u;
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    uint32_t hi = 0u;
-    const bool in = i < w1;
-    if (in) hi = keys[i] >> shift;
-    ngt += __popc(__ballot_sync(0xffffffffu, in && hi > prefix));
-    neq += __popc(__ballot_sync(0xffffffffu, in && hi == prefix));
-  }
-  if (lane == 0) {
-    wcount[warp][0] = ngt;
-    wcount[warp][1] = neq;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t g = 0u, q = 0u;
-    for (int w = 0; w < kWarps; ++w) {
-      const uint32_t a = wcount[w][0], b2 = wcount[w][1];
-      wcount[w][0] = g;
-      wcount[w][1] = q;
-      g += a;
-      q += b2;
-    }
-    cta_tot[0] = g;
-    cta_tot[1] = q;
-  }
-  __syncthreads();
-  cluster_sync_all();
-  // Carry-in of this chunk: the totals of the lower-ranked CTAs, read in
-  // parallel by warp 0 and shared through shared memory.
-  __shared__ uint32_t carry[2];
-  if (warp == 0) {
-    uint32_t cg = 0u, ce = 0u;
-    if ((uint32_t)lane < crank) {
-      cg = dsmem_ld(&cta_tot[0], (uint32_t)lane);
-      ce = dsmem_ld(&cta_tot[1], (uint32_t)lane);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      cg += __shfl_xor_sync(0xffffffffu, cg, o);
-      ce += __shfl_xor_sync(0xffffffffu, ce, o);
-    }
-    if (lane == 0) {
-      carry[0] = cg;
-      carry[1] = ce;
-    }
-  }
-  __syncthreads();
-  uint32_t g = carry[0] + wcount[warp][0];
-  uint32_t qe = carry[1] + wcount[warp][1];
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    uint32_t hi = 0u;
-    const bool in = i < w1;
-    if (in) hi = keys[i] >> shift;
-    const bool is_gt = in && hi > prefix;
-    const bool is_eq = in && hi == prefix;
-    const uint32_t bg = __ballot_sync(0xffffffffu, is_gt);
-    const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
-    const uint32_t my_g = g + __popc(bg & lt_mask);
-    const uint32_t my_e = qe + __popc(be & lt_mask);
-    if (is_gt) orow[my_g + min(my_e, take)] = (int32_t)(c0 + i);
-    else if (is_eq && my_e < take) orow[my_g + my_e] = (int32_t)(c0 + i);
-    g += __popc(bg);
-    qe += __popc(be);
-  }
-  // No CTA may exit while another can still read its shared memory.
-  cluster_sync_all();
-}
-
-
-// ---------------------------------------------------------------------------
 // Rows of up to 32768 scores: one 1024-thread CTA per row, the whole row in
 // shared memory. Every thread issues asynchronous 16-byte copies for its
 // share of the row (4-byte copies when the row start is not 16-byte
@@ -551,6 +247,7 @@ constexpr int kRowThreads = 1024;
 constexpr int kRowMaxLen = 32768;
 constexpr int kRowBins = 4096;
 constexpr int kRowGroups = 4;   // commit groups of the row copy
+constexpr int64_t kRowMinRows = 128;   // fewer rows: a cluster per row spreads each row wider
 
 struct RowSmem {
   uint32_t key[kRowMaxLen];
@@ -803,6 +500,268 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_smem_kernel(
     const int bit = __ffs(sel) - 1;
     sel &= sel - 1u;
     if (pos < (uint32_t)k) orow[pos] = base + bit;
+    ++pos;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Cluster variant, for batches too small to fill the GPU with one CTA per
+// row: the row is cut into C <= 8 contiguous chunks of at most 16384 scores,
+// one per CTA of a thread-block cluster, each held in that CTA's shared
+// memory (the row is read from HBM once).
+//
+// Elements are ranked by a 56-bit composite: the 32-bit score key above 24
+// bits of (2^24 - 1 - position), so no two elements tie and the k-th largest
+// composite alone decides the selection (equal scores go to the lower
+// positions first, as the order requires). Its top 12 bits come from
+// per-CTA 4096-bin histograms: each CTA publishes the sums of its 128
+// groups of 32 bins to every CTA of the cluster, all CTAs pick the same
+// group after one cluster barrier, then read that group's 32 bins from each
+// CTA. The remaining bits are resolved in 8-, 8-, 4-, 8-, 8- and 8-bit passes
+// (stopping as soon as the threshold bin holds exactly the keys still
+// needed), each with one cluster barrier: every CTA counts its keys of the
+// current bin into a 256-bin histogram and stores it into every CTA's
+// receive buffer (double buffered by pass parity), so after the barrier the
+// pick reads only local memory. Each CTA then marks its selected positions
+// as bitmap words, publishes its count, and after a last barrier writes its
+// positions at the offset of the CTAs before it. Every CTA of the cluster
+// runs the same barriers, so none can wait on one that has left.
+
+constexpr int kClThreads = 512;
+constexpr int kClMaxChunk = 16384;   // keys per CTA (64 KiB of shared memory)
+constexpr int kClMaxCluster = 8;
+constexpr int kClGroups = 128;       // 4096 twelve-bit bins in groups of 32
+constexpr int kClCompBits = 56;      // 32-bit key, then 24 position bits
+
+struct ClSmem {
+  uint32_t hist12[4096];                          // this CTA's 12-bit histogram
+  uint32_t gsum_in[kClMaxCluster][kClGroups];     // group sums, stored by each CTA
+  uint32_t gbins[kClMaxCluster][32];              // the picked group's bins, per CTA
+  uint32_t h8_in[2][kClMaxCluster][256];          // pass histograms, stored by each CTA
+  uint32_t h8[256];                               // this CTA's pass histogram
+  uint32_t cnt_in[kClMaxCluster];                 // selected counts, stored by each CTA
+  uint32_t wsum[32];
+  uint32_t pick[3];
+  uint32_t pad;
+  // followed by the chunk's keys (16-byte aligned)
+};
+static_assert(sizeof(ClSmem) % 16 == 0, "keys start 16-byte aligned");
+
+// Distributed shared memory: another CTA's copy of a local shared variable.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local_ptr, uint32_t rank) {
+  uint32_t remote;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;"
+      : "=r"(remote)
+      : "r"((uint32_t)__cvta_generic_to_shared(local_ptr)), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ uint32_t dsmem_ld(const uint32_t* local_ptr, uint32_t rank) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(dsmem_addr(local_ptr, rank)));
+  return v;
+}
+__device__ __forceinline__ void dsmem_st(uint32_t* local_ptr, uint32_t rank, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dsmem_addr(local_ptr, rank)), "r"(v)
+               : "memory");
+}
+// All threads of all CTAs of the cluster; shared-memory writes before it
+// (local or remote) are visible to reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// Thread t holds the count c of the t-th bin in descending order (0 past
+// the last bin). Every thread gets the position of the bin holding the
+// `take`-th largest element, that bin's count and the take within it.
+// Two block barriers.
+__device__ __forceinline__ void cl_pick(uint32_t c, uint32_t take, uint32_t* wsum, uint32_t* pick,
+                                        uint32_t& pos, uint32_t& cnt, uint32_t& take_in_bin) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kClThreads / 32;
+  uint32_t incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  const uint32_t ws = lane < kWarps ? wsum[lane] : 0u;
+  uint32_t wincl = ws;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += y;
+  }
+  const uint32_t above = __shfl_sync(0xffffffffu, wincl - ws, warp) + incl - c;
+  if (above < take && take <= above + c) {
+    pick[0] = (uint32_t)tid;
+    pick[1] = take - above;
+    pick[2] = c;
+  }
+  __syncthreads();
+  pos = pick[0];
+  take_in_bin = pick[1];
+  cnt = pick[2];
+}
+
+__global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(
+    const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ starts,
+    const int32_t* __restrict__ ends, int k, int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char cl_smem_raw[];
+  ClSmem& sm = *reinterpret_cast<ClSmem*>(cl_smem_raw);
+  uint32_t* const key = reinterpret_cast<uint32_t*>(cl_smem_raw + sizeof(ClSmem));
+  const uint32_t C = cluster_size();
+  const uint32_t rank = cluster_rank();
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  const int64_t row = blockIdx.x / C;
+  const int64_t s = starts[row];
+  const int64_t e = ends[row];
+  int L = 0;
+  if (s >= 0 && s <= stride) {
+    int64_t L64 = e - s;
+    if (L64 < 0) L64 = 0;
+    if (L64 > stride - s) L64 = stride - s;
+    L = (int)L64;   // <= C x kClMaxChunk
+  }
+  int32_t* __restrict__ orow = out + row * (int64_t)k;
+  if (L <= k) {   // the same in every CTA of the cluster: no cluster barrier is used
+    if (rank == 0)
+      for (int j = tid; j < k; j += kClThreads) orow[j] = j < L ? j : -1;
+    return;
+  }
+  const float* __restrict__ p = scores + row * stride + s;
+
+  // This CTA's chunk: positions [c0, c0 + n), chunks of a multiple of 128.
+  const int per = (int)(((int64_t)L + C - 1) / C + 127) & ~127;
+  const int c0 = min(L, (int)rank * per);
+  const int n = min(L, c0 + per) - c0;
+  const int n4 = (n + 3) >> 2;
+  if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0u) {   // c0 is a multiple of 4
+    for (int j = tid; j < n4; j += kClThreads) cp_async_16B(&key[4 * j], p + c0 + 4 * j);
+  } else {
+    for (int i = tid; i < n; i += kClThreads) cp_async_4B(&key[i], p + c0 + i);
+  }
+  cp_async_commit_group();
+  for (int i = tid; i < 4096; i += kClThreads) sm.hist12[i] = 0u;
+  cp_async_wait_group<0>();
+  __syncthreads();
+
+  uint4* const key4 = reinterpret_cast<uint4*>(key);
+  for (int j = tid; j < n4; j += kClThreads) {
+    const uint4 w = keys_of(key4[j]);
+    key4[j] = w;
+    const int valid = n - 4 * j;
+    atomicAdd(&sm.hist12[w.x >> 20], 1u);
+    if (valid > 1) atomicAdd(&sm.hist12[w.y >> 20], 1u);
+    if (valid > 2) atomicAdd(&sm.hist12[w.z >> 20], 1u);
+    if (valid > 3) atomicAdd(&sm.hist12[w.w >> 20], 1u);
+  }
+  __syncthreads();
+
+  // Group sums (thread t sums bins 8t .. 8t + 7; four threads make a group),
+  // stored into every CTA's gsum_in[rank].
+  {
+    const uint4 a = *reinterpret_cast<const uint4*>(&sm.hist12[8 * tid]);
+    const uint4 b = *reinterpret_cast<const uint4*>(&sm.hist12[8 * tid + 4]);
+    uint32_t g = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
+    g += __shfl_xor_sync(0xffffffffu, g, 1);
+    g += __shfl_xor_sync(0xffffffffu, g, 2);
+    if ((tid & 3) == 0)
+      for (uint32_t q = 0; q < C; ++q) dsmem_st(&sm.gsum_in[rank][tid >> 2], q, g);
+  }
+  cluster_sync_all();
+
+  // Threshold state: the composite's top R bits are P; `take` of the `cnt`
+  // elements with that prefix are still to be selected.
+  uint32_t take = (uint32_t)k, cnt, bpos;
+  uint32_t c = 0u;
+  if (tid < kClGroups)
+    for (uint32_t q = 0; q < C; ++q) c += sm.gsum_in[q][kClGroups - 1 - tid];
+  cl_pick(c, take, sm.wsum, sm.pick, bpos, cnt, take);
+  const int G = kClGroups - 1 - (int)bpos;
+  if (tid < 32 * (int)C) sm.gbins[tid >> 5][tid & 31] = dsmem_ld(&sm.hist12[32 * G + (tid & 31)], tid >> 5);
+  __syncthreads();
+  c = 0u;
+  if (tid < 32)
+    for (uint32_t q = 0; q < C; ++q) c += sm.gbins[q][31 - tid];
+  cl_pick(c, take, sm.wsum, sm.pick, bpos, cnt, take);
+  uint64_t P = (uint64_t)(32 * G + 31 - (int)bpos);
+  int R = 12;
+  int par = 0;
+  auto comp_of = [&](uint32_t kk, int local) -> uint64_t {
+    return ((uint64_t)kk << 24) | (uint64_t)(0xFFFFFFu - (uint32_t)(c0 + local));
+  };
+  while (cnt != take) {   // at R = 56 every composite is unique, so cnt == take == 1
+    const int width = (R >= 28 && R < 32) ? 4 : 8;
+    const int sh = kClCompBits - R, nsh = sh - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    if (tid < 256) sm.h8[tid] = 0u;
+    __syncthreads();
+    for (int j = tid; j < n4; j += kClThreads) {
+      const uint4 w = key4[j];
+      const uint32_t kk[4] = {w.x, w.y, w.z, w.w};
+      const int valid = n - 4 * j;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint64_t cp = comp_of(kk[q], 4 * j + q);
+        if (q < valid && (cp >> sh) == P) atomicAdd(&sm.h8[(uint32_t)(cp >> nsh) & dmask], 1u);
+      }
+    }
+    __syncthreads();
+    if (tid < 256)
+      for (uint32_t q = 0; q < C; ++q) dsmem_st(&sm.h8_in[par][rank][tid], q, sm.h8[tid]);
+    cluster_sync_all();
+    c = 0u;
+    if (tid <= (int)dmask)
+      for (uint32_t q = 0; q < C; ++q) c += sm.h8_in[par][q][dmask - tid];
+    cl_pick(c, take, sm.wsum, sm.pick, bpos, cnt, take);
+    P = (P << width) | (uint64_t)(dmask - bpos);
+    R += width;
+    par ^= 1;
+  }
+
+  // Selected: composite prefix >= P. Thread t owns local positions
+  // [32t, 32t + 32): 8 granules read in a lane-rotated order.
+  const int shf = kClCompBits - R;
+  const int base = 32 * tid;
+  uint32_t w = 0u;
+  if (base < n) {
+#pragma unroll
+    for (int cc0 = 0; cc0 < 8; ++cc0) {
+      const int cc = (cc0 + lane) & 7;
+      const uint4 v = key4[8 * tid + cc];
+      const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w |= (((comp_of(kk[q], base + 4 * cc + q) >> shf) >= P) ? 1u : 0u) << (4 * cc + q);
+    }
+    if (n - base < 32) w &= (1u << (n - base)) - 1u;
+  }
+  uint32_t tot;
+  uint32_t pos = block_exclusive_scan_nt<kClThreads>(__popc(w), sm.wsum, tot);
+  if (tid == 0)
+    for (uint32_t q = 0; q < C; ++q) dsmem_st(&sm.cnt_in[rank], q, tot);
+  cluster_sync_all();   // the last access to another CTA's shared memory is before this
+  for (uint32_t q = 0; q < rank; ++q) pos += sm.cnt_in[q];
+  while (w) {
+    const int bit = __ffs(w) - 1;
+    w &= w - 1u;
+    if (pos < (uint32_t)k) orow[pos] = c0 + base + bit;
     ++pos;
   }
 }
@@ -1185,11 +1144,14 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
 cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const int32_t* starts,
                         const int32_t* ends, int k, int32_t* out, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  // Many rows of up to 64K scores: one streaming CTA per row. Fewer rows
-  // (or longer ones): a cluster per row, so that one row's work is spread
-  // over several SMs. The selected set is unique, so the kernel choice never
-  // changes the output.
-  if (stride <= kRowMaxLen) {
+  // The kernel depends on the shapes alone, and the selected set is unique,
+  // so the choice never changes the output:
+  //  - enough rows of up to 32K to fill the GPU: one CTA per row, the whole
+  //    row in shared memory;
+  //  - at least 256 rows of up to 64K: the streaming grid;
+  //  - otherwise a cluster of up to 8 CTAs per row (rows of up to 128K);
+  //  - longer rows: one CTA per row with passes over global memory.
+  if (stride <= kRowMaxLen && rows >= kRowMinRows) {
     static std::atomic<bool> row_attr{false};
     if (!row_attr.load(std::memory_order_acquire)) {
       cudaError_t e = cudaFuncSetAttribute(topk_smem_kernel,
@@ -1220,24 +1182,24 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
                       sizeof(StreamSmem), stream, 1u, scores, stride, rows, starts, ends, k, out);
   }
   // Cluster size from the row stride alone: about 8K keys per CTA, at most 8
-  // CTAs. Rows longer than 8 x 16K keys take the single-CTA kernel.
+  // CTAs; chunks are multiples of 128 keys.
   int64_t C = (stride + 8191) / 8192;
-  if (C > kMaxCluster) C = kMaxCluster;
-  const int64_t per = ((stride + C - 1) / C + 3) & ~int64_t(3);
-  if (per > kMaxChunk || rows * C > (int64_t)INT32_MAX) {
+  if (C > kClMaxCluster) C = kClMaxCluster;
+  const int64_t per = ((stride + C - 1) / C + 127) & ~int64_t(127);
+  if (per > kClMaxChunk || rows * C > (int64_t)INT32_MAX) {
     return launch_pdl(topk_rows_kernel, dim3((unsigned)rows), dim3(kThreads), 0, stream, 1u, scores,
                       stride, starts, ends, k, out);
   }
-  const size_t smem = (size_t)per * sizeof(uint32_t);
+  const size_t smem = sizeof(ClSmem) + (size_t)per * sizeof(uint32_t);
   static std::atomic<bool> attr_set{false};
   if (!attr_set.load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kMaxChunk * sizeof(uint32_t)));
+                                         (int)(sizeof(ClSmem) + kClMaxChunk * sizeof(uint32_t)));
     if (e != cudaSuccess) return e;
     attr_set.store(true, std::memory_order_release);
   }
-  return launch_pdl(topk_cluster_kernel, dim3((unsigned)(rows * C)), dim3(kThreads), smem, stream,
+  return launch_pdl(topk_cluster_kernel, dim3((unsigned)(rows * C)), dim3(kClThreads), smem, stream,
                     (unsigned)C, scores, stride, starts, ends, k, out);
 }
 
