@@ -247,7 +247,7 @@ constexpr int kRowThreads = 1024;
 constexpr int kRowMaxLen = 32768;
 constexpr int kRowBins = 4096;
 constexpr int kRowGroups = 4;   // commit groups of the row copy
-constexpr int64_t kRowMinRows = 128;   // fewer rows: a cluster per row spreads each row wider
+constexpr int64_t kRowMinRows = 16;   // fewer rows: a cluster per row spreads each row wider
 
 struct RowSmem {
   uint32_t key[kRowMaxLen];
@@ -1146,8 +1146,9 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
   if (rows == 0) return cudaSuccess;
   // The kernel depends on the shapes alone, and the selected set is unique,
   // so the choice never changes the output:
-  //  - enough rows of up to 32K to fill the GPU: one CTA per row, the whole
-  //    row in shared memory;
+  //  - 16 or more rows of up to 32K: one CTA per row, the whole row in
+  //    shared memory (this leaves most SMs free, so the next kernel's CTAs
+  //    become resident while it runs);
   //  - at least 256 rows of up to 64K: the streaming grid;
   //  - otherwise a cluster of up to 8 CTAs per row (rows of up to 128K);
   //  - longer rows: one CTA per row with passes over global memory.

@@ -7,8 +7,8 @@ edge cases of "Deterministic sparse top-k" (PR 54955) and "What is fixed"
 lengths, offsets that break 16-byte alignment, rows shorter than, equal to
 and one longer than k, and empty batches. Row widths and batch sizes are
 chosen so that every kernel behind ds_topk_per_row runs: whole rows in
-shared memory (width <= 32768), the streaming grid (>= 256 rows of up to
-65536), and a cluster per row (otherwise).
+shared memory (16 or more rows of width <= 32768), the streaming grid (256
+or more rows of up to 65536), and a cluster per row (otherwise).
 """
 
 import numpy as np
