@@ -13,16 +13,17 @@
 // (query row, split of 512 entries, group of <= 64 heads). A fixed-order
 // combine kernel merges the splits. Within a CTA:
 //
-//   producer warps 4-7  gather 64-entry tiles of 1152-byte bf16 rows into a
+//   loader warps        gather 64-entry tiles of 1152-byte bf16 rows into a
 //                       128-byte-swizzled shared-memory tile (FP8 rows are
-//                       dequantised to bf16 on the way), double buffered;
-//   MMA warps 8-10      one thread each issues tcgen05 MMAs (a single thread
-//                       can issue one MMA per ~54 cycles, so three issuers
-//                       keep the tensor pipe fed):
-//                         warps 8, 10: S = Q K^T M=64 (heads), N=64, over
-//                                      dims 0-319 and 320-575 into two TMEM
-//                                      accumulators summed by the softmax
-//                         warp 9:  O^T += V^T P^T M=128 (dv block), N=heads, K=64
+//                       dequantised to bf16 on the way), double buffered:
+//                       warps 4-11 for bf16 KV, 4-7 for FP8 KV;
+//   MMA warps           the next three warps; one thread each issues tcgen05
+//                       MMAs (a single thread can issue one MMA per ~54
+//                       cycles, so three issuers keep the tensor pipe fed):
+//                         QK issuers: S = Q K^T M=64 (heads), N=64, over
+//                                     dims 0-319 and 320-575 into two TMEM
+//                                     accumulators summed by the softmax
+//                         PV issuer:  O^T += V^T P^T M=128 (dv block), N=heads, K=64
 //                       The same swizzled tile is the K-major B operand of
 //                       the first and the MN-major A operand of the second.
 //   softmax warps 0-3   read S from TMEM (one head per TMEM lane), keep a
@@ -60,12 +61,36 @@ constexpr int kTile = kTileEntries;                   // 64 entries per tile
 constexpr int kStages = 2;                            // KV tile ring
 constexpr int kStageBytes = kTile * kRowBytesBf16;    // 73728
 constexpr int kAtomStride = kTile * 128;              // bytes between 64-dim column blocks
-constexpr int kThreads = 352;                         // 11 warps
 constexpr int kSCols = kTile;                         // TMEM columns of one S buffer
 constexpr int kSbCol = 2 * kSCols;                    // second QK accumulator (2 buffers)
 constexpr int kOCol = 4 * kSCols;                     // first TMEM column of O^T
 constexpr int kQkSplitAtom = 5;                       // QK column blocks [0,5) -> S_a, [5,9) -> S_b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
+
+// Warp roles. Warps 0-3 run the softmax; then come the loader warps (eight
+// for bf16 KV, whose copies are plain cp.async; four for FP8 KV, whose
+// dequantisation needs more registers per thread); then one QK issuer, the
+// PV issuer and the second QK issuer. Loader warp pw fills rows
+// kRowsPerWarp * pw .. + kRowsPerWarp - 1 of every tile; for the page
+// lookups, lane l owns row kRowsPerWarp * pw + (l % kRowsPerWarp) of tiles
+// l / kRowsPerWarp + kTileGroups * i, i = 0 .. kSlots - 1.
+template <bool FP8>
+struct Roles {
+  static constexpr int kLoaderWarps = FP8 ? 4 : 8;
+  static constexpr int kLoaderThreads = 32 * kLoaderWarps;
+  static constexpr int kRowsPerWarp = 64 / kLoaderWarps;          // 16 or 8
+  static constexpr int kTileGroups = 32 / kRowsPerWarp;           // 2 or 4
+  static constexpr int kSlots = kSplitTiles / kTileGroups;        // 4 or 2
+  static constexpr int kQkA = 4 + kLoaderWarps;                   // also allocates TMEM
+  static constexpr int kPv = kQkA + 1;
+  static constexpr int kQkB = kQkA + 2;
+  static constexpr int kThreads = 32 * (kQkA + 3);                // 480 or 352
+};
+
+// The loader lane's KV row of slot `sel` (select chain: no local memory).
+__device__ __forceinline__ int slot_row(const int (&grow)[4], int sel) {
+  return sel == 0 ? grow[0] : sel == 1 ? grow[1] : sel == 2 ? grow[2] : grow[3];
+}
 
 // Error bits (match DS_DEVERR_* in the public header).
 constexpr int kErrIdx = 1, kErrPage = 2, kErrRowReq = 4, kErrTimeout = 8;
@@ -178,10 +203,12 @@ struct KParams {
 };
 
 template <int HG, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KParams p) {
+__global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kernel(const KParams p) {
   pdl_wait();
   pdl_trigger();
   using LY = Layout<HG>;
+  using RL = Roles<FP8>;
+  constexpr int RW = RL::kRowsPerWarp, TG = RL::kTileGroups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -195,11 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // Warps 4-7 load Q and every KV tile together: warp pw fills rows
-  // 16 pw .. 16 pw + 15 of each tile. For the page lookups, lane l of warp pw
-  // owns row 16 pw + (l & 15) of tiles (l >> 4) + 2i, i = 0..3.
-  const bool producer = warp >= 4 && warp < 8;
+  // The loader warps load Q and every KV tile together (see Roles).
+  const bool producer = warp >= 4 && warp < 4 + RL::kLoaderWarps;
   const int pw = warp - 4;
+  const int lgroup = lane / RW, lrow = lane % RW;   // tile group and row of this lane
 
   int64_t bid = blockIdx.x;
   const int hg = (int)(bid % p.num_hg);
@@ -232,41 +258,41 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       // thread; s_full: one tcgen05.commit from each QK issuer; the rest:
       // one tcgen05.commit.
       uint32_t count = 1u;
-      if (i == kQFull || i == kPFull || i == kPFull + 1) count = 128u;
+      if (i == kPFull || i == kPFull + 1) count = 128u;
+      if (i == kQFull || (i >= kKvFull && i < kKvFull + kStages)) count = RL::kLoaderThreads;
       if (i == kSFull || i == kSFull + 1) count = 2u;
-      if (i >= kKvFull && i < kKvFull + kStages) count = 128u;
       mbar_init(&bars[i], count);
     }
     mbar_fence_init();
   }
-  if (warp == 8) {
+  if (warp == RL::kQkA) {
     tmem_alloc(tmem_slot, LY::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();   // neff_s = 0 is visible before any atomicMax below
   // KV row (page * 64 + slot) of each owned entry, -1 = skip: slot i is
-  // tile (lane >> 4) + 2i, row 16 pw + (lane & 15).
+  // tile lgroup + TG i, row RW pw + lrow.
   int grow[4] = {-1, -1, -1, -1};
   if (producer) {
     const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
     const int ptid = tid - 128;
-    for (int c = ptid; c < HG * kChunks; c += 128) {
+    for (int c = ptid; c < HG * kChunks; c += RL::kLoaderThreads) {
       const int h = c / kChunks, ch = c - h * kChunks;
       cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
     }
     cp_async_commit();
-    int pos[4];
+    int pos[4] = {-1, -1, -1, -1};
     int last = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = (lane >> 4) + 2 * i;
-      pos[i] = t < ntiles ? idx_row[j0 + t * kTile + pw * 16 + (lane & 15)] : -1;
+    for (int i = 0; i < RL::kSlots; ++i) {
+      const int t = lgroup + TG * i;
+      pos[i] = t < ntiles ? idx_row[j0 + t * kTile + RW * pw + lrow] : -1;
       if (pos[i] != -1) last = t + 1;
     }
-    // All four block-table reads go out before any is used: one round trip.
+    // All block-table reads go out before any is used: one round trip.
     int64_t page[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RL::kSlots; ++i) {
       const int ps = pos[i];
       page[i] = -2;   // no lookup
       if (ps >= 0 && (int64_t)ps < len && row_ok && (int64_t)(ps >> 6) < p.bt_stride)
@@ -274,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
     }
     int err_bits = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RL::kSlots; ++i) {
       const int ps = pos[i];
       bool valid = false;
       if (ps >= 0 && (int64_t)ps < len && row_ok) {
@@ -289,9 +315,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       }
       const uint32_t ballot = __ballot_sync(0xffffffffu, valid);
       if (lane == 0) {
-        // lanes 0-15: tile 2i, lanes 16-31: tile 2i + 1; 16 rows per warp.
-        reinterpret_cast<uint16_t*>(vmask + 2 * (2 * i))[pw] = (uint16_t)(ballot & 0xFFFFu);
-        reinterpret_cast<uint16_t*>(vmask + 2 * (2 * i + 1))[pw] = (uint16_t)(ballot >> 16);
+        // Lanes RW g .. RW g + RW - 1 hold rows RW pw .. of tile g + TG i:
+        // bits RW pw .. RW pw + RW - 1 of that tile's 64-bit row mask.
+#pragma unroll
+        for (int g = 0; g < TG; ++g) {
+          const uint32_t piece = (ballot >> (RW * g)) & ((1u << RW) - 1u);
+          if constexpr (RW == 16)
+            reinterpret_cast<uint16_t*>(vmask + 2 * (g + TG * i))[pw] = (uint16_t)piece;
+          else
+            reinterpret_cast<uint8_t*>(vmask + 2 * (g + TG * i))[pw] = (uint8_t)piece;
+        }
       }
     }
     // Start tile 0 (stage 0) and stream tiles 2 and 3 into L2 right away,
@@ -302,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       const int row_bytes = FP8 ? kRowBytesFp8 : kRowBytesBf16;
       if constexpr (!FP8) {
 #pragma unroll 4
-        for (int rr = 0; rr < 16; ++rr) {
+        for (int rr = 0; rr < RW; ++rr) {   // tile 0: lanes 0 .. RW - 1, slot 0
           const int64_t g = __shfl_sync(0xffffffffu, grow[0], rr);
           const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
@@ -310,16 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
           for (int j = 0; j < 3; ++j) {
             const int c = lane + 32 * j;
             if (c < kChunks)
-              cp_async_16(stage_base + swz_off(pw * 16 + rr, c, kAtomStride), src + c * 16,
+              cp_async_16(stage_base + swz_off(RW * pw + rr, c, kAtomStride), src + c * 16,
                           nbytes);
           }
         }
         cp_async_commit();
       }
-      if ((lane >> 4) == 0 && grow[1] >= 0)   // tile 2
-        prefetch_l2_bulk(p.kv + (int64_t)grow[1] * row_bytes, (uint32_t)row_bytes);
-      if ((lane >> 4) == 1 && grow[1] >= 0)   // tile 3
-        prefetch_l2_bulk(p.kv + (int64_t)grow[1] * row_bytes, (uint32_t)row_bytes);
+#pragma unroll
+      for (int u = 2; u < 4; ++u) {   // tiles 2 and 3
+        if (u < ntiles && lgroup == u % TG) {
+          const int g = slot_row(grow, u / TG);
+          if (g >= 0) prefetch_l2_bulk(p.kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
+        }
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
@@ -343,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
     }
   } else if (producer) {
     // ------------------------------------------------------------ producers
-    // All four warps fill each tile in turn (16 rows each) into stage t & 1,
+    // All loader warps fill each tile in turn (RW rows each) into stage t & 1,
     // wait for their own copies (or stores) to land, fence them for the
     // tensor core and arrive. Q shares the first tile's wait. Shared memory
     // holds only two tiles, so L2 serves as the deeper stages: while tile t is
@@ -351,11 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
     // prefetches (tiles 2 and 3 at the start), in tile order, so each tile's
     // HBM reads overlap the compute of the tiles before it and its smem
     // copies hit L2.
-    // Rows of tile u are held by lanes with (lane >> 4) == (u & 1), slot u >> 1.
+    // Rows of tile u are held by lanes with lgroup == u % TG, slot u / TG.
     auto prefetch_tile = [&](int u, int row_bytes) {
-      if (u < n_eff && (lane >> 4) == (u & 1)) {
-        const int sel = u >> 1;
-        const int g = sel == 0 ? grow[0] : sel == 1 ? grow[1] : sel == 2 ? grow[2] : grow[3];
+      if (u < n_eff && lgroup == u % TG) {
+        const int g = slot_row(grow, u / TG);
         if (g >= 0) prefetch_l2_bulk(p.kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
       }
     };
@@ -371,12 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
         failed = true;
         break;
       }
-      const int sel = t >> 1;
-      const int gi = sel == 0 ? grow[0] : sel == 1 ? grow[1] : sel == 2 ? grow[2] : grow[3];
-      const int src_lane0 = (t & 1) << 4;
+      const int gi = slot_row(grow, t / TG);
+      const int src_lane0 = (t % TG) * RW;
       if constexpr (!FP8) {
 #pragma unroll 4
-        for (int rr = 0; rr < 16 && t > 0; ++rr) {   // tile 0 was issued in the prologue
+        for (int rr = 0; rr < RW && t > 0; ++rr) {   // tile 0 was issued in the prologue
           const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + rr);
           const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
@@ -384,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
           for (int j = 0; j < 3; ++j) {
             const int c = lane + 32 * j;
             if (c < kChunks)
-              cp_async_16(stage_base + swz_off(pw * 16 + rr, c, kAtomStride), src + c * 16,
+              cp_async_16(stage_base + swz_off(RW * pw + rr, c, kAtomStride), src + c * 16,
                           nbytes);
           }
         }
@@ -395,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
         prefetch_ahead(t, kRowBytesFp8);
         if (t == 0) cp_async_wait_all();   // Q
 #pragma unroll 1
-        for (int r0 = 0; r0 < 16; r0 += 8) {
+        for (int r0 = 0; r0 < RW; r0 += 8) {
           uint2 codes[8][2];
           float scl[8][2];
           uint4 rope[8];
@@ -419,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
           }
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const int tr = pw * 16 + r0 + u;
+            const int tr = RW * pw + r0 + u;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int c = lane + 32 * j;
@@ -435,16 +469,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
       mbar_arrive(&bars[kKvFull + stage]);
     }
     cp_async_wait_all();
-  } else if (warp == 8 || warp == 10) {
+  } else if (warp == RL::kQkA || warp == RL::kQkB) {
     // ------------------------------------------------------------ QK issuers
-    // Warp 8 accumulates column blocks [0, 5) of QK(t) into S_a, warp 10
-    // blocks [5, 9) into S_b. QK(t) needs tile t landed and its S buffers
+    // The first issuer accumulates column blocks [0, 5) of QK(t) into S_a,
+    // the second blocks [5, 9) into S_b. QK(t) needs tile t landed and its S buffers
     // free: P(t-2) written means softmax(t-2) has read S(t-2). Descriptors
     // are precomputed; each issuer's MMAs of a tile go back to back.
     if (lane == 0) {
-      const int a_lo = warp == 8 ? 0 : kQkSplitAtom;
-      const int a_hi = warp == 8 ? kQkSplitAtom : kD / 64;
-      const uint32_t s_col = warp == 8 ? 0u : (uint32_t)kSbCol;
+      const int a_lo = warp == RL::kQkA ? 0 : kQkSplitAtom;
+      const int a_hi = warp == RL::kQkA ? kQkSplitAtom : kD / 64;
+      const uint32_t s_col = warp == RL::kQkA ? 0u : (uint32_t)kSbCol;
       constexpr uint32_t idesc_qk = make_idesc_bf16(64, kTile, 0, 0);
       const uint64_t q_desc = make_sw128_desc(sbase + LY::kQ, 16, 1024);
       const uint64_t kv_desc0 = make_sw128_desc(sbase + LY::kKV, 16, 1024);
@@ -471,12 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
         }
         mma_commit(&bars[kSFull + sb]);
       }
-      const int done_bar = kMmaDone + (warp == 8 ? 0 : 2);
+      const int done_bar = kMmaDone + (warp == RL::kQkA ? 0 : 2);
       mma_commit(&bars[done_bar]);
       mbar_wait(&bars[done_bar], 0);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == RL::kPv) {
     // ------------------------------------------------------------ PV issuer
     // PV(t) needs P(t); its completion frees the KV stage and lets softmax
     // overwrite P and rescale O^T.
@@ -635,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_split_kernel(const KPa
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 8) tmem_dealloc(tmem, LY::kTmemCols);
+  if (warp == RL::kQkA) tmem_dealloc(tmem, LY::kTmemCols);
 }
 
 // Merges the splits of one (row, head) in split order: M = max m_s,
@@ -708,7 +742,8 @@ cudaError_t launch_split(const KParams& kp, int64_t blocks, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     attr_set.store(true, std::memory_order_release);
   }
-  return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), LY::kSmemBytes, stream, 1u, kp);
+  return launch_pdl(kern, dim3((unsigned)blocks), dim3(Roles<FP8>::kThreads), LY::kSmemBytes, stream,
+                    1u, kp);
 }
 
 }  // namespace
