@@ -16,7 +16,7 @@
 //   loader warps        gather 64-entry tiles of 1152-byte bf16 rows into a
 //                       128-byte-swizzled shared-memory tile (FP8 rows are
 //                       dequantised to bf16 on the way), double buffered:
-//                       warps 4-11 for bf16 KV, 4-7 for FP8 KV;
+//                       warps 4-11;
 //   MMA warps           the next three warps; one thread each issues tcgen05
 //                       MMAs (a single thread can issue one MMA per ~54
 //                       cycles, so three issuers keep the tensor pipe fed):
@@ -67,24 +67,22 @@ constexpr int kOCol = 4 * kSCols;                     // first TMEM column of O^
 constexpr int kQkSplitAtom = 5;                       // QK column blocks [0,5) -> S_a, [5,9) -> S_b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 
-// Warp roles. Warps 0-3 run the softmax; then come the loader warps (eight
-// for bf16 KV, whose copies are plain cp.async; four for FP8 KV, whose
-// dequantisation needs more registers per thread); then one QK issuer, the
-// PV issuer and the second QK issuer. Loader warp pw fills rows
+// Warp roles. Warps 0-3 run the softmax; warps 4-11 load; then come one QK
+// issuer, the PV issuer and the second QK issuer. Loader warp pw fills rows
 // kRowsPerWarp * pw .. + kRowsPerWarp - 1 of every tile; for the page
 // lookups, lane l owns row kRowsPerWarp * pw + (l % kRowsPerWarp) of tiles
 // l / kRowsPerWarp + kTileGroups * i, i = 0 .. kSlots - 1.
 template <bool FP8>
 struct Roles {
-  static constexpr int kLoaderWarps = FP8 ? 4 : 8;
+  static constexpr int kLoaderWarps = 8;
   static constexpr int kLoaderThreads = 32 * kLoaderWarps;
-  static constexpr int kRowsPerWarp = 64 / kLoaderWarps;          // 16 or 8
-  static constexpr int kTileGroups = 32 / kRowsPerWarp;           // 2 or 4
-  static constexpr int kSlots = kSplitTiles / kTileGroups;        // 4 or 2
+  static constexpr int kRowsPerWarp = 64 / kLoaderWarps;          // 8
+  static constexpr int kTileGroups = 32 / kRowsPerWarp;           // 4
+  static constexpr int kSlots = kSplitTiles / kTileGroups;        // 2
   static constexpr int kQkA = 4 + kLoaderWarps;                   // also allocates TMEM
   static constexpr int kPv = kQkA + 1;
   static constexpr int kQkB = kQkA + 2;
-  static constexpr int kThreads = 32 * (kQkA + 3);                // 480 or 352
+  static constexpr int kThreads = 32 * (kQkA + 3);                // 480
 };
 
 // The loader lane's KV row of slot `sel` (select chain: no local memory).
