@@ -50,6 +50,10 @@ WORKLOAD_DESCS = {
     "chunked_prefill": ("chunked sparse MLA prefill: 1 request, 4096 query tokens at positions "
                         "61440..65535 of a 65536 context, causal, topk 2048, 128 heads, bf16 KV, "
                         "fp32 N(0,1) scores"),
+    "tp2_mtp4_decode": ("MTP4 sparse MLA decode: 32 requests x 5 query tokens (1 target + 4 draft), "
+                        "64 heads, request lengths uniform int in [4096, 32768], token j of a "
+                        "request sees seq_len - 4 + j positions, topk 2048, bf16 KV, fp32 N(0,1) "
+                        "scores"),
 }
 METRIC = "sparse-MLA decode tokens/s and top-k rows/s on 1 GB300; % of roofline"
 N_SETS = 4
@@ -237,7 +241,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     sets = []
     n_sets = args.sets
-    from synthetic import WORKLOADS, decode_case, prefill_case, _uniform_ints
+    from synthetic import WORKLOADS, decode_case, prefill_case, mtp_case, _uniform_ints
     wl = args.workload
     w = WORKLOADS[wl]
     for s in range(n_sets):
@@ -248,6 +252,12 @@ def run_ours(args, rank, world, local):
                                 else seed)
             c = decode_case(wl, ctx, w["H"], w["k"], w["kv"], seed if s or rank else w["seed"],
                             w["scores"], stride=w["stride"], device="cuda")
+        elif w["kind"] == "mtp":
+            lens = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if s == 0 and rank == 0
+                                 else seed)
+            c = mtp_case(wl, lens, w["next_n"], w["H"], w["k"], w["kv"],
+                         seed if s or rank else w["seed"], w["scores"], stride=w["stride"],
+                         device="cuda")
         else:
             c = prefill_case(wl, w["ctx"], w["first_pos"], w["T"], w["H"], w["k"], w["kv"],
                              seed if s or rank else w["seed"], device="cuda")
@@ -509,7 +519,7 @@ def oracle_sample_inputs(case, rows):
     scores = case.scores[rows].cpu().numpy()
     starts = case.row_starts.cpu().numpy()[rows]
     ends = case.row_ends.cpu().numpy()[rows]
-    bt = case.block_table.cpu().numpy()[rows]
+    bt = case.block_table.cpu().numpy()[case.row_req.cpu().numpy()[rows]]   # each row's table row
     q = case.q[rows].cpu().view(torch.int16).numpy().view(np.uint16)
     used = np.unique(bt[bt >= 0])
     remap = np.zeros(int(used.max()) + 1 if used.size else 1, dtype=np.int64)

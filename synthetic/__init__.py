@@ -196,6 +196,36 @@ def prefill_case(name, ctx, first_pos, T, H, k, kv_dtype="bf16", seed=3, device=
                                          "stride": ctx})
 
 
+def mtp_case(name, seq_lens, next_n, H, k, kv_dtype="bf16", seed=5, score_mode="normal",
+             stride=None, device="cpu", scale=None):
+    """Multi-token decode: ``next_n`` query tokens per request (one target
+    token and next_n - 1 draft tokens), every token reading its request's
+    block-table row.
+
+    Token j of request r scores the context [0, seq_lens[r] - next_n + 1 + j).
+    That length is signed: it is negative for the first tokens of a padded
+    request (seq_lens[r] == 0), and the top-k clamps it to an empty row.
+    """
+    seq_lens = [int(x) for x in seq_lens]
+    B = len(seq_lens)
+    R = B * next_n
+    ends = [sl - next_n + 1 + j for sl in seq_lens for j in range(next_n)]
+    stride = int(stride if stride is not None else max(1, max(seq_lens)))
+    g = _gen(seed, device)
+    bt, num_pages = _block_table([max(1, sl) for sl in seq_lens], g, device)
+    starts = torch.zeros(R, dtype=torch.int32, device=device)
+    ends_t = torch.tensor(ends, dtype=torch.int32, device=device)
+    scores = _scores(R, stride, [0] * R, ends, score_mode, g, device)
+    q = _normal((R, H, D_QK), g, device).to(torch.bfloat16)
+    kv = _kv_pool(num_pages, kv_dtype, g, device)
+    row_req = torch.arange(B, dtype=torch.int32, device=device).repeat_interleave(next_n)
+    return Case(name=name, H=H, k=k, kv_dtype=kv_dtype,
+                scale=float(scale if scale is not None else 1.0 / math.sqrt(D_QK)),
+                scores=scores, row_starts=starts, row_ends=ends_t, q=q, kv_pages=kv,
+                block_table=bt, row_req=row_req, lens=ends_t.clamp(min=0),
+                meta={"seq_lens": seq_lens, "next_n": next_n, "seed": seed, "stride": stride})
+
+
 def _uniform_ints(lo, hi, n, seed):
     g = torch.Generator().manual_seed(int(seed) + 1000003)
     return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
@@ -211,6 +241,9 @@ WORKLOADS = {
                            scores="normal", seed=2, stride=131072),
     "chunked_prefill": dict(kind="prefill", T=4096, H=128, ctx=65536, first_pos=61440, k=2048,
                             kv="bf16", scores="normal", seed=3),
+    # MTP4 decode: one target and four draft tokens per request.
+    "tp2_mtp4_decode": dict(kind="mtp", B=32, next_n=5, H=64, ctx=(4096, 32768), k=2048,
+                            kv="bf16", scores="normal", seed=5, stride=32768),
 }
 
 
@@ -223,6 +256,12 @@ def workload_case(name, device="cpu", rows=None):
         ctx = [lo] * B if lo == hi else _uniform_ints(lo, hi, w["B"], w["seed"])[:B]
         return decode_case(name, ctx, w["H"], w["k"], w["kv"], w["seed"], w["scores"],
                            stride=w.get("stride"), device=device)
+    if w["kind"] == "mtp":
+        lo, hi = w["ctx"]
+        B = w["B"] if rows is None else int(rows)
+        return mtp_case(name, _uniform_ints(lo, hi, w["B"], w["seed"])[:B], w["next_n"], w["H"],
+                        w["k"], w["kv"], w["seed"], w["scores"], stride=w.get("stride"),
+                        device=device)
     T = w["T"] if rows is None else int(rows)
     return prefill_case(name, w["ctx"], w["ctx"] - T if rows is not None else w["first_pos"],
                         T, w["H"], w["k"], w["kv"], w["seed"], device)
