@@ -28,7 +28,13 @@ valid entry returns its V row exactly).
 """
 
 from .topk import score_key, row_length, topk_per_row, topk_rank_bruteforce  # noqa: F401
-from .fp8 import e4m3_to_float64, bf16_bits_to_float64  # noqa: F401
+from .fp8 import (  # noqa: F401
+    e4m3_to_float64,
+    bf16_bits_to_float64,
+    e4m3_encode,
+    quantize_latent_rows,
+    kv_cache_write,
+)
 from .attention import (  # noqa: F401
     gather_latent_rows,
     sparse_mla_rows,
