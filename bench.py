@@ -50,6 +50,9 @@ WORKLOAD_DESCS = {
     "chunked_prefill": ("chunked sparse MLA prefill: 1 request, 4096 query tokens at positions "
                         "61440..65535 of a 65536 context, causal, topk 2048, 128 heads, bf16 KV, "
                         "fp32 N(0,1) scores"),
+    "fp8_cache_write": ("FP8 KV cache write: 65536 new bf16 latent rows (576 dims) quantised to the "
+                        "656-byte E4M3 layout (fp32 scale per 128 dims, bf16 rope) at randomly "
+                        "permuted slots of a 1024-page pool"),
     "tp2_mtp4_decode": ("MTP4 sparse MLA decode: 32 requests x 5 query tokens (1 target + 4 draft), "
                         "64 heads, request lengths uniform int in [4096, 32768], token j of a "
                         "request sees seq_len - 4 + j positions, topk 2048, bf16 KV, fp32 N(0,1) "
@@ -601,11 +604,103 @@ def run_reference(args, rank, world):
             "gpu_launches": 0}
 
 
+def run_cache_write(args, rank, world, local):
+    """The KV cache write alone: `value` in rows/s, roofline against HBM.
+
+    Algorithmic bytes per row: 1152 read (bf16 latent) + 656 written (FP8
+    row) + 8 read (the slot). Four rotating input sets (latent rows and
+    slots), each writing a random permutation of a pool's slots; 4 x 75 MB of
+    latent rows against 129 MB of L2.
+    """
+    import torch
+    import invariant_sparse_mla_gb300 as ds
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    N, pages = 65536, 1024
+    sets = []
+    for s in range(args.sets):
+        g = torch.Generator(device=dev).manual_seed(100 + 1000 * rank + s)
+        lat = torch.randn((N, 576), generator=g, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(pages * 64, generator=g, device=dev)[:N].to(torch.int64)
+        pool = torch.zeros((pages, 64, 656), dtype=torch.uint8, device=dev)
+        sets.append((lat, slots, pool))
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(c):
+        ds.kv_cache_write(c[0], c[1], c[2], "fp8", stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for c in sets:
+                step(c)
+    stream.synchronize()
+    gph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gph, stream=stream):
+        for c in sets:
+            step(c)
+    reps = max(1, math.ceil(args.steps / len(sets)))
+    for _ in range(max(1, math.ceil(max(args.warmup, 3) / len(sets)))):
+        with torch.cuda.stream(stream):
+            gph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id_for_smi(local))
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            gph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    t1 = time.time()
+    barrier(world)
+    sampler.stop()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    steps = reps * len(sets)
+    per_call = secs / steps
+    hbm, _, peak_kind = load_peaks()
+    row_bytes = 1152 + 656 + 8
+    gbs = N * row_bytes / per_call / 1e9
+    line = {"metric": METRIC + " [fp8_cache_write]", "value": round(world * N / per_call, 1),
+            "unit": "rows/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(per_call * 1e3, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 -> e4m3", "data": "synthetic (seeded N(0,1) rows)",
+            "config": {"workload": WORKLOAD_DESCS["fp8_cache_write"], "rows": N, "pages": pages,
+                       "l2": f"{args.sets} rotating input sets, "
+                             f"{args.sets * N * 1152 // 2**20} MB of latent rows vs 129 MB L2",
+                       "cuda_graph": True},
+            "roofline": {"bound": "hbm", "kernel": "kv_write_fp8_kernel", "achieved": round(gbs, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                         "peak_kind": f"{peak_kind} HBM copy", "traffic": None,
+                         "algorithmic_bytes": N * row_bytes},
+            "gpu_launches": steps, "clocks": sampler.summary(t0, t1)}
+    if rank == 0 and not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        bits = sets[0][0][:4096].cpu().view(torch.int16).numpy().view(np.uint16)
+        t = time.perf_counter()
+        n_done = 0
+        while time.perf_counter() - t < 5.0:
+            oracle.quantize_latent_rows(bits)
+            n_done += bits.shape[0]
+        dt = time.perf_counter() - t
+        line["cpu_baseline"] = {"value": round(n_done / dt, 1), "unit": "rows/s",
+                                "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                "sample": f"{n_done} rows of input set 0 quantised by the oracle "
+                                          f"({dt:.1f} s)"}
+    return line
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload == "fp8_cache_write":
+        line = run_cache_write(args, rank, world, local)
     else:
         line = run_ours(args, rank, world, local)
     if rank == 0 and line is not None:

@@ -230,6 +230,36 @@ int ds_sparse_mla_decode_noalloc(const void* q, const void* kv_pages, int kv_dty
                                  int num_heads, int k, float scale, void* out, float* lse,
                                  int32_t* err_flag, void* stream);
 
+/*
+ * KV cache write: new latent rows into the paged cache, as bf16 rows or
+ * quantised to the FP8 layout above (MooreThreads/vllm-musa PR 178,
+ * optimisation table: the FP8 attention cache write, with each row's FP32
+ * scale groups kept contiguous).
+ *
+ *  latent     bfloat16 [num_rows, 576] (512 latent dims, then 64 rope dims),
+ *             16-byte aligned.
+ *  slots      int64 [num_rows], 8-byte aligned: row i goes to slot
+ *             page * 64 + offset ("[Bugfix] Make DSV4 sparse MLA work
+ *             end-to-end ...", section "What is fixed": slot =
+ *             block_id * block_size + offset). A negative slot is a padding
+ *             row and writes nothing (never into page 0); a slot at or past
+ *             num_pages * 64 writes nothing and ORs DS_DEVERR_PAGE into
+ *             err_flag.
+ *  kv_dtype   DS_KV_BF16: the row is copied. DS_KV_FP8_E4M3: per group of
+ *             128 latent dims, scale = amax / 448 (1 for an all-zero group),
+ *             code = E4M3(x / scale) rounded to nearest, ties to even,
+ *             saturating at +-448 (float32 division); the four float32
+ *             scales and the 64 bf16 rope dims follow the codes.
+ *  kv_pages   the pool (layout as for ds_sparse_mla_decode), 16-byte aligned;
+ *             only the written slots change.
+ *  err_flag   optional int32 device word (NULL = no report).
+ *
+ * Rows are independent: a row's bytes depend on that row alone. num_rows = 0
+ * is a no-op. Slots that repeat are written in an unspecified order.
+ */
+int ds_kv_cache_write(const void* latent, int64_t num_rows, const int64_t* slots, int kv_dtype,
+                      void* kv_pages, int64_t num_pages, int32_t* err_flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

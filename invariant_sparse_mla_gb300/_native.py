@@ -67,13 +67,15 @@ def lib():
         L.ds_sparse_mla_decode_noalloc.restype = i32
         L.ds_sparse_mla_decode_noalloc.argtypes = [vp, vp, i32, i64, vp, i64, vp, vp, i64, i32,
                                                    i32, f32, vp, vp, vp, vp]
+        L.ds_kv_cache_write.restype = i32
+        L.ds_kv_cache_write.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
         _lib = L
         return _lib
 
 
 EXPORTED = ("ds_last_error", "ds_supported_config", "ds_topk_workspace_size",
             "ds_sparse_mla_workspace_size", "ds_topk_per_row", "ds_sparse_mla_decode",
-            "ds_sparse_mla_prefill", "ds_sparse_mla_decode_noalloc")
+            "ds_sparse_mla_prefill", "ds_sparse_mla_decode_noalloc", "ds_kv_cache_write")
 
 
 def last_error():
@@ -206,3 +208,33 @@ def sparse_mla_prefill(q, kv_pages, kv_dtype, block_table, row_req, idx, lens, s
         _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_flag),
         _stream(stream, dev)))
     return out, lse
+
+
+def kv_cache_write(latent, slots, kv_pages, kv_dtype, err_flag=None, stream=None):
+    """Write new latent rows (bf16 [N, 576]) into the paged pool at ``slots``
+    (int64 [N], page * 64 + offset; negative = padding); FP8 pools get the
+    quantised layout. Returns ``kv_pages``."""
+    _need(latent, "latent", torch.bfloat16, ndim=2)
+    dev = latent.device
+    if latent.shape[1] != 576:
+        raise ValueError("latent must be [rows, 576]")
+    _need(slots, "slots", torch.int64, dev, 1)
+    if slots.numel() != latent.shape[0]:
+        raise ValueError("slots must have one entry per latent row")
+    kvd = KV_DTYPES.get(kv_dtype)
+    if kvd is None:
+        raise ValueError(f"kv_dtype must be 'bf16' or 'fp8', got {kv_dtype!r}")
+    if kvd == 0:
+        _need(kv_pages, "kv_pages", torch.bfloat16, dev, 3)
+        if tuple(kv_pages.shape[1:]) != (64, 576):
+            raise ValueError("bf16 kv_pages must be [num_pages, 64, 576]")
+    else:
+        _need(kv_pages, "kv_pages", torch.uint8, dev, 3)
+        if tuple(kv_pages.shape[1:]) != (64, 656):
+            raise ValueError("fp8 kv_pages must be [num_pages, 64, 656] bytes")
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32, dev)
+    _check(lib().ds_kv_cache_write(_ptr(latent), latent.shape[0], _ptr(slots), kvd,
+                                   _ptr(kv_pages), kv_pages.shape[0], _ptr(err_flag),
+                                   _stream(stream, dev)))
+    return kv_pages

@@ -225,4 +225,34 @@ int ds_sparse_mla_prefill(const void* q, const void* kv_pages, int kv_dtype, int
                           scale, out, lse, workspace, workspace_bytes, err_flag, stream);
 }
 
+int ds_kv_cache_write(const void* latent, int64_t num_rows, const int64_t* slots, int kv_dtype,
+                      void* kv_pages, int64_t num_pages, int32_t* err_flag, void* stream) {
+  const char* fn = "ds_kv_cache_write";
+  if (kv_dtype != DS_KV_BF16 && kv_dtype != DS_KV_FP8_E4M3)
+    return fail(DS_ERR_DTYPE, "%s: kv_dtype=%d must be DS_KV_BF16 (0) or DS_KV_FP8_E4M3 (1)", fn,
+                kv_dtype);
+  if (num_rows < 0) return fail(DS_ERR_SHAPE, "%s: num_rows=%lld must be >= 0", fn, (long long)num_rows);
+  if (num_pages < 1) return fail(DS_ERR_SHAPE, "%s: num_pages=%lld must be >= 1", fn, (long long)num_pages);
+  if (num_pages > INT64_MAX / (DS_PAGE_BLOCK_SIZE * (int64_t)DS_KV_ROW_BYTES_BF16))
+    return fail(DS_ERR_UNSUPPORTED, "%s: num_pages=%lld is too large", fn, (long long)num_pages);
+  if (num_rows == 0) return ok();
+  struct {
+    const void* p;
+    const char* name;
+    uintptr_t align;
+  } ptrs[] = {{latent, "latent", 16}, {slots, "slots", 8}, {kv_pages, "kv_pages", 16}};
+  for (auto& x : ptrs) {
+    if (x.p == nullptr) return fail(DS_ERR_NULL, "%s: %s is NULL", fn, x.name);
+    if (!aligned(x.p, x.align))
+      return fail(DS_ERR_ALIGN, "%s: %s must be %d-byte aligned", fn, x.name, (int)x.align);
+  }
+  if (err_flag != nullptr && !aligned(err_flag, 4))
+    return fail(DS_ERR_ALIGN, "%s: err_flag must be 4-byte aligned", fn);
+  cudaError_t e = dsmla::launch_kv_cache_write(latent, num_rows, slots, kv_dtype, kv_pages,
+                                               num_pages, err_flag,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
 }  // extern "C"

@@ -53,6 +53,10 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
 
 cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream);
 
+cudaError_t launch_kv_cache_write(const void* latent, int64_t n, const int64_t* slots,
+                                  int kv_dtype, void* pool, int64_t num_pages, int32_t* err,
+                                  cudaStream_t stream);
+
 // ---- programmatic dependent launch. Every kernel of this library is
 // launched with the programmatic-stream-serialization attribute, so it may
 // become resident while the previous kernel of the stream is still running.

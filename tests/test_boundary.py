@@ -163,3 +163,20 @@ def test_python_binding_fails_loudly_without_cuda_tensors(ds):
     with pytest.raises(TypeError):
         ds.topk_per_row(torch.zeros(2, 8, dtype=torch.float64), torch.zeros(2, dtype=torch.int32),
                         torch.zeros(2, dtype=torch.int32), 4)
+
+
+def _write(L, latent=A, n=4, slots=A, kvd=1, pool=A, pages=16, err=None):
+    return L.ds_kv_cache_write(latent, n, slots, kvd, pool, pages, err, None)
+
+
+def test_kv_cache_write_rejects_bad_arguments(L):
+    assert _write(L, kvd=3) == DS_ERR_DTYPE and "kv_dtype" in _err(L)
+    assert _write(L, n=-1) == DS_ERR_SHAPE and "num_rows" in _err(L)
+    assert _write(L, pages=0) == DS_ERR_SHAPE and "num_pages" in _err(L)
+    assert _write(L, latent=None) == DS_ERR_NULL and "latent" in _err(L)
+    assert _write(L, slots=None) == DS_ERR_NULL and "slots" in _err(L)
+    assert _write(L, pool=None) == DS_ERR_NULL and "kv_pages" in _err(L)
+    assert _write(L, latent=A + 8) == DS_ERR_ALIGN and "latent" in _err(L)
+    assert _write(L, slots=A + 4) == DS_ERR_ALIGN and "slots" in _err(L)
+    # Zero rows is a valid empty call: nothing is launched.
+    assert _write(L, n=0, latent=None, slots=None) == DS_OK
