@@ -40,4 +40,6 @@ from .attention import (  # noqa: F401
     sparse_mla_rows,
     sparse_mla_decode,
     sparse_mla_prefill,
+    sparse_mla_rows_sink,
+    sparse_mla_decode_swa,
 )

@@ -141,3 +141,72 @@ def sparse_mla_prefill(q_bits, kv_pages, kv_dtype, block_table, row_req, idx, le
     T = q_bits.shape[0]
     rows = list(range(T)) if rows is None else list(rows)
     return _rows(q_bits, kv_pages, kv_dtype, block_table, row_req, idx, lens, scale, rows)
+
+
+def sparse_mla_rows_sink(q_rows, K, scale, sink):
+    """Attention of H query rows over n latent rows plus one sink logit per head.
+
+    The sink of head h is a logit ``sink[h]`` (natural-log units, the same
+    units as ``scale * q . K``) that joins the softmax denominator with no
+    value row; ``-inf`` means no sink:
+
+        out[h, :] = sum_j exp(S[h, j]) V[j, :] / (sum_j exp(S[h, j]) + exp(sink[h]))
+        lse[h]    = log(sum_j exp(S[h, j]) + exp(sink[h]))
+
+    A head with no valid entry and no sink gives out = 0 and lse = -inf; with
+    a sink and no entry, out = 0 and lse = sink.
+    """
+    H = q_rows.shape[0]
+    sink = np.asarray(sink, dtype=np.float64)
+    S = scale * (q_rows @ K.T) if K.shape[0] else np.zeros((H, 0))
+    out = np.zeros((H, D_V))
+    lse = np.full(H, -np.inf)
+    for h in range(H):
+        logits = np.concatenate([S[h], [sink[h]]])
+        m = logits.max()
+        if m == -np.inf:
+            continue
+        w = np.exp(logits - m)                       # the sink's weight is w[-1]
+        denom = w.sum()
+        out[h] = (w[:-1] @ K[:, :D_V]) / denom if K.shape[0] else 0.0
+        lse[h] = m + np.log(denom)
+    return out, lse
+
+
+def sparse_mla_decode_swa(q_bits, kv_pages, kv_dtype, block_table, idx, lens,
+                          swa_pages, swa_block_table, swa_idx, swa_lens, sink, scale, rows=None):
+    """Decode over the concatenation [top-k entries of the compressed KV ||
+    sliding-window entries of the window KV], with a per-head attention sink.
+
+    "[DeepSeek-V4][Preview][DO NOT MERGE] Batch-invariant kernels for 0-diff
+    RL", section "Sparse MLA and FlashMLA": decode gathers compressed and
+    sliding-window KV and runs one sparse attention over both; the section
+    on model loading keeps -inf padding in the attention sinks. "[Bugfix]
+    Make DSV4 sparse MLA work end-to-end ...", section "What is fixed": the
+    window index list is padded to a multiple of 64 entries (-1 padding).
+
+    Readings where the pages are silent: the window entries are positions
+    in their own paged pool (same row format and element type as the
+    compressed pool), looked up through their own block table and valid iff
+    ``0 <= swa_idx < swa_lens[row]``; ``sink`` is float [H] in natural-log
+    units (``None`` or -inf: no sink). Attention is the plain definition of
+    ``sparse_mla_rows_sink`` over all valid entries of both lists.
+    """
+    B, H = q_bits.shape[0], q_bits.shape[1]
+    rows = list(range(B)) if rows is None else list(rows)
+    sink = np.full(H, -np.inf) if sink is None else np.asarray(sink, dtype=np.float64)
+    out = np.zeros((len(rows), H, D_V))
+    lse = np.full((len(rows), H), -np.inf)
+    for i, r in enumerate(rows):
+        parts = []
+        for pages, bt, ix, ln in ((kv_pages, block_table, idx, lens),
+                                  (swa_pages, swa_block_table, swa_idx, swa_lens)):
+            if pages is None or ix is None:
+                continue
+            ent = _valid_entries(ix[r], ln[r], bt[r], pages.shape[0])
+            if ent:
+                parts.append(gather_latent_rows(pages, kv_dtype, bt[r], ent))
+        K = np.concatenate(parts) if parts else np.zeros((0, D_QK))
+        q = bf16_bits_to_float64(q_bits[r])
+        out[i], lse[i] = sparse_mla_rows_sink(q, K, scale, sink)
+    return out, lse
