@@ -231,6 +231,53 @@ int ds_sparse_mla_decode_noalloc(const void* q, const void* kv_pages, int kv_dty
                                  int32_t* err_flag, void* stream);
 
 /*
+ * Sparse MLA decode over the concatenation [top-k entries of the compressed
+ * KV || sliding-window entries of the window KV], with per-head attention
+ * sinks ("[DeepSeek-V4][Preview][DO NOT MERGE] Batch-invariant kernels for
+ * 0-diff RL", section "Sparse MLA and FlashMLA": decode gathers compressed
+ * and sliding-window KV and runs one sparse attention over both; attention
+ * sinks keep -inf padding. "[Bugfix] Make DSV4 sparse MLA work end-to-end
+ * ...", section "What is fixed": the window index list is padded to a
+ * multiple of 64 entries).
+ *
+ * The first ten arguments and q, out, lse, workspace, err_flag and stream
+ * are those of ds_sparse_mla_decode (k is the top-k width). The window:
+ *  swa_pages        the window pool, same row format and kv_dtype as
+ *                   kv_pages, 16-byte aligned; swa_num_pages >= 1.
+ *  swa_block_table  int32 [num_rows, swa_bt_stride]: page id of each
+ *                   64-position block of the row's window context.
+ *  swa_idx          int32 [num_rows, swa_width]: window positions (-1 =
+ *                   padding); an entry is valid iff 0 <= swa_idx < swa_lens[row]
+ *                   and its page lookup hits, like a top-k entry.
+ *  swa_lens         int32 [num_rows].
+ *  swa_width        0 (no window; the window arguments may be NULL) or a
+ *                   multiple of 64 in [64, 512].
+ *  attn_sink        optional float32 [num_heads] (NULL = no sinks): the sink
+ *                   logit of each head, in the units of scale * q.K (natural
+ *                   log). It joins the softmax denominator with no value row:
+ *                   out = sum_j exp(S_j) V_j / (sum_j exp(S_j) + exp(sink)),
+ *                   lse = log(sum_j exp(S_j) + exp(sink)); -inf = no sink.
+ *                   A head with no valid entry gives out = 0 and lse = sink.
+ *  workspace        >= ds_sparse_mla_swa_workspace_size(num_rows, num_heads,
+ *                   k, swa_width) bytes, 256-byte aligned.
+ *
+ * The window entries form their own split(s) after the top-k splits, so the
+ * reduction order depends on k and swa_width only, never on the batch.
+ */
+int ds_sparse_mla_decode_swa(const void* q, const void* kv_pages, int kv_dtype, int64_t num_pages,
+                             const int32_t* block_table, int64_t bt_stride, const int32_t* idx,
+                             const int32_t* lens, int k, const void* swa_pages,
+                             int64_t swa_num_pages, const int32_t* swa_block_table,
+                             int64_t swa_bt_stride, const int32_t* swa_idx,
+                             const int32_t* swa_lens, int swa_width, const float* attn_sink,
+                             int64_t num_rows, int num_heads, float scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                             void* stream);
+
+/* Workspace bytes of ds_sparse_mla_decode_swa (0 for an unsupported shape). */
+size_t ds_sparse_mla_swa_workspace_size(int64_t num_rows, int num_heads, int k, int swa_width);
+
+/*
  * KV cache write: new latent rows into the paged cache, as bf16 rows or
  * quantised to the FP8 layout above (MooreThreads/vllm-musa PR 178,
  * optimisation table: the FP8 attention cache write, with each row's FP32

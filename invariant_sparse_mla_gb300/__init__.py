@@ -18,7 +18,9 @@ from ._native import (  # noqa: F401
     last_error,
     lib,
     sparse_mla_decode,
+    sparse_mla_decode_swa,
     sparse_mla_prefill,
     supported_config,
+    swa_workspace_size,
     topk_per_row,
 )

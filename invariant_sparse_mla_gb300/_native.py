@@ -67,6 +67,12 @@ def lib():
         L.ds_sparse_mla_decode_noalloc.restype = i32
         L.ds_sparse_mla_decode_noalloc.argtypes = [vp, vp, i32, i64, vp, i64, vp, vp, i64, i32,
                                                    i32, f32, vp, vp, vp, vp]
+        L.ds_sparse_mla_decode_swa.restype = i32
+        L.ds_sparse_mla_decode_swa.argtypes = [vp, vp, i32, i64, vp, i64, vp, vp, i32, vp, i64,
+                                               vp, i64, vp, vp, i32, vp, i64, i32, f32, vp, vp,
+                                               vp, sz, vp, vp]
+        L.ds_sparse_mla_swa_workspace_size.restype = sz
+        L.ds_sparse_mla_swa_workspace_size.argtypes = [i64, i32, i32, i32]
         L.ds_kv_cache_write.restype = i32
         L.ds_kv_cache_write.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
         _lib = L
@@ -75,7 +81,8 @@ def lib():
 
 EXPORTED = ("ds_last_error", "ds_supported_config", "ds_topk_workspace_size",
             "ds_sparse_mla_workspace_size", "ds_topk_per_row", "ds_sparse_mla_decode",
-            "ds_sparse_mla_prefill", "ds_sparse_mla_decode_noalloc", "ds_kv_cache_write")
+            "ds_sparse_mla_prefill", "ds_sparse_mla_decode_noalloc", "ds_kv_cache_write",
+            "ds_sparse_mla_decode_swa", "ds_sparse_mla_swa_workspace_size")
 
 
 def last_error():
@@ -238,3 +245,44 @@ def kv_cache_write(latent, slots, kv_pages, kv_dtype, err_flag=None, stream=None
                                    _ptr(kv_pages), kv_pages.shape[0], _ptr(err_flag),
                                    _stream(stream, dev)))
     return kv_pages
+
+
+def swa_workspace_size(num_rows, num_heads, k, swa_width):
+    return int(lib().ds_sparse_mla_swa_workspace_size(num_rows, num_heads, k, swa_width))
+
+
+def sparse_mla_decode_swa(q, kv_pages, kv_dtype, block_table, idx, lens, scale, swa_pages=None,
+                          swa_block_table=None, swa_idx=None, swa_lens=None, attn_sink=None,
+                          out=None, lse=None, workspace=None, err_flag=None, stream=None):
+    """Decode over [top-k entries || sliding-window entries] with optional
+    per-head sinks (float32 [H], natural log); returns (out, lse)."""
+    dev, R, H, k, kvd, out, lse, _ = _attention_args(
+        q, kv_pages, kv_dtype, block_table, idx, lens, out, lse, torch.empty(0, dtype=torch.uint8,
+                                                                             device=q.device),
+        err_flag)
+    W = 0
+    if swa_idx is not None:
+        W = swa_idx.shape[1]
+        _need(swa_idx, "swa_idx", torch.int32, dev, 2)
+        _need(swa_lens, "swa_lens", torch.int32, dev, 1)
+        _need(swa_block_table, "swa_block_table", torch.int32, dev, 2)
+        _need(swa_pages, "swa_pages", kv_pages.dtype, dev, 3)
+        if tuple(swa_pages.shape[1:]) != tuple(kv_pages.shape[1:]):
+            raise ValueError("swa_pages must have the row format of kv_pages")
+        if swa_idx.shape[0] != R or swa_lens.numel() != R or swa_block_table.shape[0] != R:
+            raise ValueError("the window arguments must have one row per query row")
+    if attn_sink is not None:
+        _need(attn_sink, "attn_sink", torch.float32, dev, 1)
+        if attn_sink.numel() != H:
+            raise ValueError("attn_sink must have num_heads entries")
+    need = swa_workspace_size(R, H, k, W) if R > 0 else 0
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    _check(lib().ds_sparse_mla_decode_swa(
+        _ptr(q), _ptr(kv_pages), kvd, kv_pages.shape[0], _ptr(block_table), block_table.shape[1],
+        _ptr(idx), _ptr(lens), k, _ptr(swa_pages), swa_pages.shape[0] if W else 0,
+        _ptr(swa_block_table), swa_block_table.shape[1] if W else 0, _ptr(swa_idx),
+        _ptr(swa_lens), W, _ptr(attn_sink), R, H, float(scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream, dev)))
+    return out, lse

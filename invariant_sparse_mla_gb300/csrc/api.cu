@@ -62,17 +62,39 @@ int check_config(const char* fn, int num_heads, int topk, int page_block_size, i
   return DS_OK;
 }
 
+// The optional second entry list (a sliding window) and the sinks.
+struct Window {
+  const void* pages = nullptr;
+  int64_t num_pages = 0;
+  const int32_t* block_table = nullptr;
+  int64_t bt_stride = 0;
+  const int32_t* idx = nullptr;
+  const int32_t* lens = nullptr;
+  int width = 0;
+  const float* sink = nullptr;
+};
+
+int check_window(const char* fn, const Window& w) {
+  if (w.width != 0 && (w.width < 64 || w.width > 512 || w.width % 64 != 0))
+    return fail(DS_ERR_UNSUPPORTED,
+                "%s: swa_width=%d is not supported; available: 0 or a multiple of 64 in [64, 512]",
+                fn, w.width);
+  return DS_OK;
+}
+
 int attention_common(const char* fn, const void* q, const void* kv_pages, int kv_dtype,
                      int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
                      int64_t num_bt_rows, const int32_t* row_req, const int32_t* idx,
                      const int32_t* lens, int64_t num_rows, int num_heads, int k, float scale,
                      void* out, float* lse, void* workspace, size_t workspace_bytes,
-                     int32_t* err_flag, void* stream) {
+                     int32_t* err_flag, void* stream, const Window& win = Window()) {
   int st = check_config(fn, num_heads, k, DS_PAGE_BLOCK_SIZE, DS_D_QK, DS_D_V, kv_dtype);
+  if (st != DS_OK) return st;
+  st = check_window(fn, win);
   if (st != DS_OK) return st;
   if (num_rows < 0) return fail(DS_ERR_SHAPE, "%s: num_rows=%lld is negative", fn, (long long)num_rows);
   if (num_rows == 0) return ok();
-  const int64_t splits = dsmla::num_splits_for_k(k);
+  const int64_t splits = dsmla::num_splits_total(k, win.width);
   const int64_t groups = num_heads > 64 ? num_heads / 64 : 1;
   if (num_rows > (int64_t)INT32_MAX / (splits * groups) || num_rows * num_heads > (int64_t)INT32_MAX)
     return fail(DS_ERR_UNSUPPORTED, "%s: num_rows=%lld is too large for one launch (max %lld)", fn,
@@ -101,7 +123,29 @@ int attention_common(const char* fn, const void* q, const void* kv_pages, int kv
     return fail(DS_ERR_ALIGN, "%s: row_req must be 4-byte aligned", fn);
   if (err_flag != nullptr && !aligned(err_flag, 4))
     return fail(DS_ERR_ALIGN, "%s: err_flag must be 4-byte aligned", fn);
-  const size_t need = dsmla::attn_workspace_bytes(num_rows, num_heads, k);
+  if (win.width > 0) {
+    if (win.num_pages < 1)
+      return fail(DS_ERR_SHAPE, "%s: swa_num_pages=%lld must be >= 1", fn, (long long)win.num_pages);
+    if (win.num_pages > (int64_t)INT32_MAX / DS_PAGE_BLOCK_SIZE)
+      return fail(DS_ERR_UNSUPPORTED, "%s: swa_num_pages=%lld exceeds %lld", fn,
+                  (long long)win.num_pages, (long long)(INT32_MAX / DS_PAGE_BLOCK_SIZE));
+    if (win.bt_stride < 1)
+      return fail(DS_ERR_SHAPE, "%s: swa_bt_stride=%lld must be >= 1", fn, (long long)win.bt_stride);
+    struct {
+      const void* p;
+      const char* name;
+      uintptr_t align;
+    } wp[] = {{win.pages, "swa_pages", 16}, {win.block_table, "swa_block_table", 4},
+              {win.idx, "swa_idx", 4}, {win.lens, "swa_lens", 4}};
+    for (auto& x : wp) {
+      if (x.p == nullptr) return fail(DS_ERR_NULL, "%s: %s is NULL", fn, x.name);
+      if (!aligned(x.p, x.align))
+        return fail(DS_ERR_ALIGN, "%s: %s must be %d-byte aligned", fn, x.name, (int)x.align);
+    }
+  }
+  if (win.sink != nullptr && !aligned(win.sink, 4))
+    return fail(DS_ERR_ALIGN, "%s: attn_sink must be 4-byte aligned", fn);
+  const size_t need = dsmla::attn_workspace_bytes(num_rows, num_heads, k, win.width);
   if (workspace_bytes < need)
     return fail(DS_ERR_WORKSPACE, "%s: workspace_bytes=%zu is smaller than the %zu bytes needed", fn,
                 workspace_bytes, need);
@@ -125,6 +169,14 @@ int attention_common(const char* fn, const void* q, const void* kv_pages, int kv
   a.lse = lse;
   a.workspace = workspace;
   a.err_flag = err_flag;
+  a.kv2 = win.pages;
+  a.num_pages2 = win.num_pages;
+  a.block_table2 = win.block_table;
+  a.bt_stride2 = win.bt_stride;
+  a.idx2 = win.idx;
+  a.lens2 = win.lens;
+  a.k2 = win.width;
+  a.sink = win.sink;
   cudaError_t e = dsmla::launch_sparse_mla(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();
@@ -253,6 +305,41 @@ int ds_kv_cache_write(const void* latent, int64_t num_rows, const int64_t* slots
                                                reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();
+}
+
+size_t ds_sparse_mla_swa_workspace_size(int64_t num_rows, int num_heads, int k, int swa_width) {
+  if (num_rows < 0) return 0;
+  if (check_config("ds_sparse_mla_swa_workspace_size", num_heads, k, DS_PAGE_BLOCK_SIZE, DS_D_QK,
+                   DS_D_V, DS_KV_BF16) != DS_OK)
+    return 0;
+  Window w;
+  w.width = swa_width;
+  if (check_window("ds_sparse_mla_swa_workspace_size", w) != DS_OK) return 0;
+  return dsmla::attn_workspace_bytes(num_rows, num_heads, k, swa_width);
+}
+
+int ds_sparse_mla_decode_swa(const void* q, const void* kv_pages, int kv_dtype, int64_t num_pages,
+                             const int32_t* block_table, int64_t bt_stride, const int32_t* idx,
+                             const int32_t* lens, int k, const void* swa_pages,
+                             int64_t swa_num_pages, const int32_t* swa_block_table,
+                             int64_t swa_bt_stride, const int32_t* swa_idx,
+                             const int32_t* swa_lens, int swa_width, const float* attn_sink,
+                             int64_t num_rows, int num_heads, float scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                             void* stream) {
+  Window w;
+  w.pages = swa_pages;
+  w.num_pages = swa_num_pages;
+  w.block_table = swa_block_table;
+  w.bt_stride = swa_bt_stride;
+  w.idx = swa_idx;
+  w.lens = swa_lens;
+  w.width = swa_width;
+  w.sink = attn_sink;
+  return attention_common("ds_sparse_mla_decode_swa", q, kv_pages, kv_dtype, num_pages,
+                          block_table, bt_stride, num_rows < 1 ? 1 : num_rows, nullptr, idx, lens,
+                          num_rows, num_heads, k, scale, out, lse, workspace, workspace_bytes,
+                          err_flag, stream, w);
 }
 
 }  // extern "C"

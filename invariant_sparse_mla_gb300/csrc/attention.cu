@@ -194,6 +194,16 @@ struct KParams {
   int num_splits;
   int num_hg;
   float scale_log2;
+  // Second entry list (sliding window): splits num_splits1 .. num_splits - 1
+  // read it instead of the top-k list.
+  const uint8_t* kv2;
+  int64_t num_pages2;
+  const int32_t* block_table2;
+  int64_t bt_stride2;
+  const int32_t* idx2;
+  const int32_t* lens2;
+  int k2;
+  int num_splits1;
   float* part_o;
   float* part_m;
   float* part_l;
@@ -237,13 +247,22 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     bt_row = p.row_req[row];
     row_ok = bt_row >= 0 && bt_row < p.num_bt_rows;
   }
-  int64_t len = p.lens[row];
+  // The entry list of this split: the top-k list into the main pool, or,
+  // for splits past the top-k ones, the second list into its own pool.
+  const bool second = split >= p.num_splits1;
+  const uint8_t* const kv = second ? p.kv2 : p.kv;
+  const int64_t num_pages = second ? p.num_pages2 : p.num_pages;
+  const int32_t* const block_table = second ? p.block_table2 : p.block_table;
+  const int64_t bt_stride = second ? p.bt_stride2 : p.bt_stride;
+  const int klist = second ? p.k2 : p.k;
+  const int lsplit = second ? split - p.num_splits1 : split;
+  int64_t len = (second ? p.lens2 : p.lens)[row];
   if (len < 0) len = 0;
 
-  const int j0 = split * kSplitEntries;
-  const int j1 = min(p.k, j0 + kSplitEntries);
+  const int j0 = lsplit * kSplitEntries;
+  const int j1 = min(klist, j0 + kSplitEntries);
   const int ntiles = (j1 - j0) / kTile;
-  const int32_t* idx_row = p.idx + row * (int64_t)p.k;
+  const int32_t* idx_row = (second ? p.idx2 : p.idx) + row * (int64_t)klist;
   const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
 
   // ---- prologue (one block-wide barrier): producers start the Q copies,
@@ -293,8 +312,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     for (int i = 0; i < RL::kSlots; ++i) {
       const int ps = pos[i];
       page[i] = -2;   // no lookup
-      if (ps >= 0 && (int64_t)ps < len && row_ok && (int64_t)(ps >> 6) < p.bt_stride)
-        page[i] = p.block_table[bt_row * p.bt_stride + (ps >> 6)];
+      if (ps >= 0 && (int64_t)ps < len && row_ok && (int64_t)(ps >> 6) < bt_stride)
+        page[i] = block_table[bt_row * bt_stride + (ps >> 6)];
     }
     int err_bits = 0;
 #pragma unroll
@@ -302,7 +321,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       const int ps = pos[i];
       bool valid = false;
       if (ps >= 0 && (int64_t)ps < len && row_ok) {
-        if (page[i] >= 0 && page[i] < p.num_pages) {
+        if (page[i] >= 0 && page[i] < num_pages) {
           grow[i] = (int)(page[i] * 64 + (ps & 63));
           valid = true;
         } else {
@@ -335,7 +354,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 #pragma unroll 4
         for (int rr = 0; rr < RW; ++rr) {   // tile 0: lanes 0 .. RW - 1, slot 0
           const int64_t g = __shfl_sync(0xffffffffu, grow[0], rr);
-          const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
+          const uint8_t* src = kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
@@ -351,7 +370,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       for (int u = 2; u < 4; ++u) {   // tiles 2 and 3
         if (u < ntiles && lgroup == u % TG) {
           const int g = slot_row(grow, u / TG);
-          if (g >= 0) prefetch_l2_bulk(p.kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
+          if (g >= 0) prefetch_l2_bulk(kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
         }
       }
     }
@@ -389,7 +408,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     auto prefetch_tile = [&](int u, int row_bytes) {
       if (u < n_eff && lgroup == u % TG) {
         const int g = slot_row(grow, u / TG);
-        if (g >= 0) prefetch_l2_bulk(p.kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
+        if (g >= 0) prefetch_l2_bulk(kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
       }
     };
     auto prefetch_ahead = [&](int t, int row_bytes) {
@@ -410,7 +429,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 #pragma unroll 4
         for (int rr = 0; rr < RW && t > 0; ++rr) {   // tile 0 was issued in the prologue
           const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + rr);
-          const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
+          const uint8_t* src = kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
@@ -434,7 +453,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + r0 + u);
-            const uint8_t* src = p.kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesFp8;
+            const uint8_t* src = kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesFp8;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int c = lane + 32 * j;  // latent output chunk 0..63
@@ -670,16 +689,19 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   if (warp == RL::kQkA) tmem_dealloc(tmem, LY::kTmemCols);
 }
 
-// Merges the splits of one (row, head) in split order: M = max m_s,
-// out = sum 2^(m_s - M) O_s / sum 2^(m_s - M) l_s, lse = (M + log2 L) ln 2.
-// Every split's m, l and O slice is loaded in one round (there are at most
-// kMaxSplits) before any arithmetic, so the loads overlap.
-constexpr int kMaxSplits = 2048 / kSplitEntries;
+// Merges the splits of one (row, head) in split order: M = max(m_s, sink),
+// L = sum 2^(m_s - M) l_s + 2^(sink - M), out = sum 2^(m_s - M) O_s / L,
+// lse = (M + log2 L) ln 2, all in log2 units (the sink logit s becomes
+// s log2 e). The sink joins the denominator only, after the splits, and -inf
+// (or no sink array) leaves the sum as it is. Every split's m, l and O slice
+// is loaded in one round (at most kMaxSplits) before any arithmetic.
+constexpr int kMaxSplits = 8;
 
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
                                                       const float* __restrict__ part_m,
                                                       const float* __restrict__ part_l,
                                                       int64_t R, int H, int S,
+                                                      const float* __restrict__ sink,
                                                       __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ lse) {
   pdl_wait();
@@ -700,7 +722,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
       os[s] = *reinterpret_cast<const float4*>(part_o + (s * RH + rh) * kDv + 4 * t);
     }
   }
-  float M = -INFINITY;
+  const float sl = sink != nullptr ? sink[rh % H] * 1.4426950408889634f : -INFINITY;
+  float M = sl;
 #pragma unroll
   for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ms[s]);
   __nv_bfloat16* o = out + rh * kDv + 4 * t;
@@ -721,6 +744,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     acc[2] += w * os[s].z;
     acc[3] += w * os[s].w;
   }
+  if (sl != -INFINITY) L += ex2(sl - M);
   const float inv = 1.0f / L;
   uint2 r;
   r.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
@@ -746,16 +770,16 @@ cudaError_t launch_split(const KParams& kp, int64_t blocks, cudaStream_t stream)
 
 }  // namespace
 
-size_t attn_workspace_bytes(int64_t R, int H, int k) {
-  const int64_t S = num_splits_for_k(k);
+size_t attn_workspace_bytes(int64_t R, int H, int k, int k2) {
+  const int64_t S = num_splits_total(k, k2);
   const int64_t n = S * R * H;
   const size_t o = (size_t)n * kDv * sizeof(float);
   const size_t ml = ((size_t)n * sizeof(float) + 255) & ~size_t(255);
   return o + 2 * ml;
 }
 
-AttnWorkspace attn_workspace_carve(void* base, int64_t R, int H, int k) {
-  const int64_t S = num_splits_for_k(k);
+AttnWorkspace attn_workspace_carve(void* base, int64_t R, int H, int k, int k2) {
+  const int64_t S = num_splits_total(k, k2);
   const int64_t n = S * R * H;
   const size_t o = (size_t)n * kDv * sizeof(float);
   const size_t ml = ((size_t)n * sizeof(float) + 255) & ~size_t(255);
@@ -782,10 +806,18 @@ cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream) {
   kp.R = a.R;
   kp.H = a.H;
   kp.k = a.k;
-  kp.num_splits = num_splits_for_k(a.k);
+  kp.num_splits1 = num_splits_for_k(a.k);
+  kp.num_splits = num_splits_total(a.k, a.k2);
+  kp.kv2 = reinterpret_cast<const uint8_t*>(a.kv2);
+  kp.num_pages2 = a.num_pages2;
+  kp.block_table2 = a.block_table2;
+  kp.bt_stride2 = a.bt_stride2;
+  kp.idx2 = a.idx2;
+  kp.lens2 = a.lens2;
+  kp.k2 = a.k2;
   kp.num_hg = a.H / HG;
   kp.scale_log2 = a.scale * 1.4426950408889634f;
-  AttnWorkspace ws = attn_workspace_carve(a.workspace, a.R, a.H, a.k);
+  AttnWorkspace ws = attn_workspace_carve(a.workspace, a.R, a.H, a.k, a.k2);
   kp.part_o = ws.part_o;
   kp.part_m = ws.part_m;
   kp.part_l = ws.part_l;
@@ -802,7 +834,7 @@ cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   return launch_pdl(combine_kernel, dim3((unsigned)(a.R * a.H)), dim3(128), 0, stream, 1u,
                     (const float*)ws.part_o, (const float*)ws.part_m, (const float*)ws.part_l, a.R,
-                    a.H, kp.num_splits, reinterpret_cast<__nv_bfloat16*>(a.out), a.lse);
+                    a.H, kp.num_splits, a.sink, reinterpret_cast<__nv_bfloat16*>(a.out), a.lse);
 }
 
 }  // namespace dsmla

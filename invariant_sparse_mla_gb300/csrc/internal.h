@@ -17,6 +17,12 @@ constexpr int kSplitEntries = kTileEntries * kSplitTiles;
 
 inline int num_splits_for_k(int k) { return (k + kSplitEntries - 1) / kSplitEntries; }
 
+// Splits of a call whose rows also attend to `k2` entries of a second list
+// (a sliding window): the top-k splits, then the second list's own splits.
+inline int num_splits_total(int k, int k2) {
+  return num_splits_for_k(k) + (k2 > 0 ? num_splits_for_k(k2) : 0);
+}
+
 struct AttnArgs {
   const void* q;             // bf16 [R, H, 576]
   const void* kv;            // pool base
@@ -36,6 +42,16 @@ struct AttnArgs {
   float* lse;                // [R, H]
   void* workspace;
   int32_t* err_flag;         // may be nullptr
+  // Optional second entry list into a second pool (a sliding window), with
+  // its own block table: k2 entries per row, 0 = none.
+  const void* kv2 = nullptr;
+  int64_t num_pages2 = 0;
+  const int32_t* block_table2 = nullptr;
+  int64_t bt_stride2 = 0;
+  const int32_t* idx2 = nullptr;   // [R, k2]
+  const int32_t* lens2 = nullptr;  // [R]
+  int k2 = 0;
+  const float* sink = nullptr;     // [H] per-head sink logits (natural log), may be nullptr
 };
 
 // Workspace layout of the attention path: partial O, m and l per split.
@@ -45,8 +61,8 @@ struct AttnWorkspace {
   float* part_l;  // [S, R, H]
 };
 
-size_t attn_workspace_bytes(int64_t R, int H, int k);
-AttnWorkspace attn_workspace_carve(void* base, int64_t R, int H, int k);
+size_t attn_workspace_bytes(int64_t R, int H, int k, int k2 = 0);
+AttnWorkspace attn_workspace_carve(void* base, int64_t R, int H, int k, int k2 = 0);
 
 cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const int32_t* starts,
                         const int32_t* ends, int k, int32_t* out, cudaStream_t stream);
