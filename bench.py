@@ -50,6 +50,10 @@ WORKLOAD_DESCS = {
     "chunked_prefill": ("chunked sparse MLA prefill: 1 request, 4096 query tokens at positions "
                         "61440..65535 of a 65536 context, causal, topk 2048, 128 heads, bf16 KV, "
                         "fp32 N(0,1) scores"),
+    "tp2_decode_swa": ("TP2-shaped sparse MLA decode over [top-k 2048 compressed entries || a "
+                       "128-entry sliding window of a second pool] with per-head attention sinks: "
+                       "batch 32, 64 heads, contexts uniform int in [4096, 32768], bf16 KV, fp32 "
+                       "N(0,1) scores"),
     "fp8_cache_write": ("FP8 KV cache write: 65536 new bf16 latent rows (576 dims) quantised to the "
                         "656-byte E4M3 layout (fp32 scale per 128 dims, bf16 rope) at randomly "
                         "permuted slots of a 1024-page pool"),
@@ -231,6 +235,10 @@ def algorithmic_bytes(case, idx):
     row_bytes = 1152 if case.kv_dtype == "bf16" else 656
     R, H = case.q.shape[0], case.q.shape[1]
     attn = distinct * row_bytes + case.q.numel() * 2 + R * H * 512 * 2 + R * H * 4 + idx.numel() * 4
+    if getattr(case, "win", None) is not None:   # window entries: distinct per row
+        wvalid = int(((case.win[2] >= 0) & (case.win[2] < case.win[3][:, None])).sum())
+        attn += wvalid * row_bytes + case.win[2].numel() * 4
+        valid += wvalid
     flops = 2 * valid * H * (576 + 512)
     return topk, attn, flops
 
@@ -244,17 +252,22 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     sets = []
     n_sets = args.sets
-    from synthetic import WORKLOADS, decode_case, prefill_case, mtp_case, _uniform_ints
+    from synthetic import WORKLOADS, decode_case, prefill_case, mtp_case, window_case, _uniform_ints
     wl = args.workload
     w = WORKLOADS[wl]
     for s in range(n_sets):
         # Independent batches per set and rank: the same recipe, shifted seeds.
         seed = w["seed"] + 1000 * rank + 17 * s
-        if w["kind"] == "decode":
+        if w["kind"] in ("decode", "decode_swa"):
             ctx = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if s == 0 and rank == 0
                                 else seed)
             c = decode_case(wl, ctx, w["H"], w["k"], w["kv"], seed if s or rank else w["seed"],
                             w["scores"], stride=w["stride"], device="cuda")
+            if w["kind"] == "decode_swa":
+                # The window cache holds each request's last swa_width tokens.
+                c.win = window_case([min(n, w["swa_width"]) for n in ctx], w["swa_width"], w["kv"],
+                                    seed + 7, device="cuda")
+                c.sink = torch.randn(w["H"], generator=torch.Generator().manual_seed(seed)).cuda()
         elif w["kind"] == "mtp":
             lens = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if s == 0 and rank == 0
                                  else seed)
@@ -268,7 +281,8 @@ def run_ours(args, rank, world, local):
         c.idx = torch.empty((R, k), dtype=torch.int32, device=dev)
         c.out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
         c.lse = torch.empty((R, H), dtype=torch.float32, device=dev)
-        c.ws = torch.empty(ds.attention_workspace_size(R, H, k), dtype=torch.uint8, device=dev)
+        c.ws = torch.empty(ds.swa_workspace_size(R, H, k, w.get("swa_width", 0)),
+                           dtype=torch.uint8, device=dev)
         sets.append(c)
     R, H, k = sets[0].q.shape[0], sets[0].H, sets[0].k
     stream = torch.cuda.Stream(device=dev)
@@ -280,6 +294,11 @@ def run_ours(args, rank, world, local):
         if w["kind"] == "decode":
             ds.sparse_mla_decode(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.idx, c.lens,
                                  c.scale, out=c.out, lse=c.lse, workspace=c.ws, stream=stream)
+        elif w["kind"] == "decode_swa":
+            ds.sparse_mla_decode_swa(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.idx, c.lens,
+                                     c.scale, swa_pages=c.win[0], swa_block_table=c.win[1],
+                                     swa_idx=c.win[2], swa_lens=c.win[3], attn_sink=c.sink,
+                                     out=c.out, lse=c.lse, workspace=c.ws, stream=stream)
         else:
             ds.sparse_mla_prefill(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.row_req, c.idx,
                                   c.lens, c.scale, out=c.out, lse=c.lse, workspace=c.ws,

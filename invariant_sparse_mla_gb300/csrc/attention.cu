@@ -64,6 +64,7 @@ constexpr int kAtomStride = kTile * 128;              // bytes between 64-dim co
 constexpr int kSCols = kTile;                         // TMEM columns of one S buffer
 constexpr int kSbCol = 2 * kSCols;                    // second QK accumulator (2 buffers)
 constexpr int kOCol = 4 * kSCols;                     // first TMEM column of O^T
+constexpr int kMaxSplitTiles = 12;                    // tiles one split may hold
 constexpr int kQkSplitAtom = 5;                       // QK column blocks [0,5) -> S_a, [5,9) -> S_b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 
@@ -78,7 +79,7 @@ struct Roles {
   static constexpr int kLoaderThreads = 32 * kLoaderWarps;
   static constexpr int kRowsPerWarp = 64 / kLoaderWarps;          // 8
   static constexpr int kTileGroups = 32 / kRowsPerWarp;           // 4
-  static constexpr int kSlots = kSplitTiles / kTileGroups;        // 2
+  static constexpr int kSlots = kMaxSplitTiles / kTileGroups;    // 3
   static constexpr int kQkA = 4 + kLoaderWarps;                   // also allocates TMEM
   static constexpr int kPv = kQkA + 1;
   static constexpr int kQkB = kQkA + 2;
@@ -101,8 +102,8 @@ struct Layout {
   static constexpr int kP = kKV + kStages * kStageBytes;      // HG rows x 128 B (64 entries)
   static constexpr int kPBytes = HG * 128;
   static constexpr int kBars = kP + kPBytes;                  // 16 x u64
-  static constexpr int kMask = kBars + 16 * 8;                // kSplitTiles x u64
-  static constexpr int kAlpha = kMask + kSplitTiles * 8;      // 2 x 64 floats
+  static constexpr int kMask = kBars + 16 * 8;                // kMaxSplitTiles x u64
+  static constexpr int kAlpha = kMask + kMaxSplitTiles * 8;   // 2 x 64 floats
   static constexpr int kTmemSlot = kAlpha + 2 * 64 * 4;       // u32
   static constexpr int kNeff = kTmemSlot + 4;                 // int
   static constexpr int kEnd = kNeff + 12;
@@ -194,8 +195,8 @@ struct KParams {
   int num_splits;
   int num_hg;
   float scale_log2;
-  // Second entry list (sliding window): splits num_splits1 .. num_splits - 1
-  // read it instead of the top-k list.
+  // Second entry list (sliding window), read through its own pool and block
+  // table; its tiles follow the top-k tiles in the concatenated list.
   const uint8_t* kv2;
   int64_t num_pages2;
   const int32_t* block_table2;
@@ -203,7 +204,6 @@ struct KParams {
   const int32_t* idx2;
   const int32_t* lens2;
   int k2;
-  int num_splits1;
   float* part_o;
   float* part_m;
   float* part_l;
@@ -247,22 +247,22 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     bt_row = p.row_req[row];
     row_ok = bt_row >= 0 && bt_row < p.num_bt_rows;
   }
-  // The entry list of this split: the top-k list into the main pool, or,
-  // for splits past the top-k ones, the second list into its own pool.
-  const bool second = split >= p.num_splits1;
-  const uint8_t* const kv = second ? p.kv2 : p.kv;
-  const int64_t num_pages = second ? p.num_pages2 : p.num_pages;
-  const int32_t* const block_table = second ? p.block_table2 : p.block_table;
-  const int64_t bt_stride = second ? p.bt_stride2 : p.bt_stride;
-  const int klist = second ? p.k2 : p.k;
-  const int lsplit = second ? split - p.num_splits1 : split;
-  int64_t len = (second ? p.lens2 : p.lens)[row];
-  if (len < 0) len = 0;
-
-  const int j0 = lsplit * kSplitEntries;
-  const int j1 = min(klist, j0 + kSplitEntries);
-  const int ntiles = (j1 - j0) / kTile;
-  const int32_t* idx_row = (second ? p.idx2 : p.idx) + row * (int64_t)klist;
+  // The concatenated entry list [top-k list || second list] in 64-entry
+  // tiles: tile u < T1 holds top-k entries 64u .. 64u + 63 (main pool), tile
+  // u >= T1 entries 64(u - T1) .. of the second list (its own pool). Split s
+  // owns tiles [floor(s T / S), floor((s + 1) T / S)): a function of k and
+  // the second list's width alone, never of the batch.
+  const int T1 = p.k / kTile;
+  const int T = T1 + p.k2 / kTile;
+  const int u0 = (int)((int64_t)split * T / p.num_splits);
+  const int ntiles = (int)((int64_t)(split + 1) * T / p.num_splits) - u0;
+  int64_t len1 = p.lens[row], len2 = p.k2 > 0 ? p.lens2[row] : 0;
+  if (len1 < 0) len1 = 0;
+  if (len2 < 0) len2 = 0;
+  const int32_t* idx_row1 = p.idx + row * (int64_t)p.k;
+  const int32_t* idx_row2 = p.k2 > 0 ? p.idx2 + row * (int64_t)p.k2 : nullptr;
+  // Pool of local tile t (tiles never straddle the two lists).
+  auto tile_kv = [&](int t) { return u0 + t >= T1 ? p.kv2 : p.kv; };
   const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
 
   // ---- prologue (one block-wide barrier): producers start the Q copies,
@@ -299,11 +299,17 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     }
     cp_async_commit();
     int pos[4] = {-1, -1, -1, -1};
+    bool sec[4] = {false, false, false, false};   // slot's tile is in the second list
     int last = 0;
 #pragma unroll
     for (int i = 0; i < RL::kSlots; ++i) {
       const int t = lgroup + TG * i;
-      pos[i] = t < ntiles ? idx_row[j0 + t * kTile + RW * pw + lrow] : -1;
+      if (t < ntiles) {
+        const int u = u0 + t;
+        sec[i] = u >= T1;
+        pos[i] = sec[i] ? idx_row2[(u - T1) * kTile + RW * pw + lrow]
+                        : idx_row1[u * kTile + RW * pw + lrow];
+      }
       if (pos[i] != -1) last = t + 1;
     }
     // All block-table reads go out before any is used: one round trip.
@@ -311,17 +317,20 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 #pragma unroll
     for (int i = 0; i < RL::kSlots; ++i) {
       const int ps = pos[i];
+      const int64_t len = sec[i] ? len2 : len1;
+      const int64_t bts = sec[i] ? p.bt_stride2 : p.bt_stride;
       page[i] = -2;   // no lookup
-      if (ps >= 0 && (int64_t)ps < len && row_ok && (int64_t)(ps >> 6) < bt_stride)
-        page[i] = block_table[bt_row * bt_stride + (ps >> 6)];
+      if (ps >= 0 && (int64_t)ps < len && row_ok && (int64_t)(ps >> 6) < bts)
+        page[i] = (sec[i] ? p.block_table2 : p.block_table)[bt_row * bts + (ps >> 6)];
     }
     int err_bits = 0;
 #pragma unroll
     for (int i = 0; i < RL::kSlots; ++i) {
       const int ps = pos[i];
+      const int64_t len = sec[i] ? len2 : len1;
       bool valid = false;
       if (ps >= 0 && (int64_t)ps < len && row_ok) {
-        if (page[i] >= 0 && page[i] < num_pages) {
+        if (page[i] >= 0 && page[i] < (sec[i] ? p.num_pages2 : p.num_pages)) {
           grow[i] = (int)(page[i] * 64 + (ps & 63));
           valid = true;
         } else {
@@ -354,7 +363,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 #pragma unroll 4
         for (int rr = 0; rr < RW; ++rr) {   // tile 0: lanes 0 .. RW - 1, slot 0
           const int64_t g = __shfl_sync(0xffffffffu, grow[0], rr);
-          const uint8_t* src = kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
+          const uint8_t* src = tile_kv(0) + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
@@ -370,7 +379,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       for (int u = 2; u < 4; ++u) {   // tiles 2 and 3
         if (u < ntiles && lgroup == u % TG) {
           const int g = slot_row(grow, u / TG);
-          if (g >= 0) prefetch_l2_bulk(kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
+          if (g >= 0) prefetch_l2_bulk(tile_kv(u) + (int64_t)g * row_bytes, (uint32_t)row_bytes);
         }
       }
     }
@@ -408,7 +417,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     auto prefetch_tile = [&](int u, int row_bytes) {
       if (u < n_eff && lgroup == u % TG) {
         const int g = slot_row(grow, u / TG);
-        if (g >= 0) prefetch_l2_bulk(kv + (int64_t)g * row_bytes, (uint32_t)row_bytes);
+        if (g >= 0) prefetch_l2_bulk(tile_kv(u) + (int64_t)g * row_bytes, (uint32_t)row_bytes);
       }
     };
     auto prefetch_ahead = [&](int t, int row_bytes) {
@@ -429,7 +438,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 #pragma unroll 4
         for (int rr = 0; rr < RW && t > 0; ++rr) {   // tile 0 was issued in the prologue
           const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + rr);
-          const uint8_t* src = kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
+          const uint8_t* src = tile_kv(t) + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
           const uint32_t nbytes = g >= 0 ? 16u : 0u;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + r0 + u);
-            const uint8_t* src = kv + (g >= 0 ? g : 0) * (int64_t)kRowBytesFp8;
+            const uint8_t* src = tile_kv(t) + (g >= 0 ? g : 0) * (int64_t)kRowBytesFp8;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int c = lane + 32 * j;  // latent output chunk 0..63
@@ -695,7 +704,12 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 // s log2 e). The sink joins the denominator only, after the splits, and -inf
 // (or no sink array) leaves the sum as it is. Every split's m, l and O slice
 // is loaded in one round (at most kMaxSplits) before any arithmetic.
-constexpr int kMaxSplits = 8;
+// Largest split count: top-k 2048 (4 splits of 512), or 2048 + 512 window
+// entries at most 768 per split (4).
+constexpr int kMaxSplits = 4;
+static_assert((2048 + kSplitEntries - 1) / kSplitEntries <= kMaxSplits &&
+                  (2048 + 512 + 767) / 768 <= kMaxSplits,
+              "every split of the largest call is merged");
 
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
                                                       const float* __restrict__ part_m,
@@ -806,7 +820,6 @@ cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream) {
   kp.R = a.R;
   kp.H = a.H;
   kp.k = a.k;
-  kp.num_splits1 = num_splits_for_k(a.k);
   kp.num_splits = num_splits_total(a.k, a.k2);
   kp.kv2 = reinterpret_cast<const uint8_t*>(a.kv2);
   kp.num_pages2 = a.num_pages2;

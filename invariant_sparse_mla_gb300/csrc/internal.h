@@ -18,9 +18,14 @@ constexpr int kSplitEntries = kTileEntries * kSplitTiles;
 inline int num_splits_for_k(int k) { return (k + kSplitEntries - 1) / kSplitEntries; }
 
 // Splits of a call whose rows also attend to `k2` entries of a second list
-// (a sliding window): the top-k splits, then the second list's own splits.
+// (a sliding window): as many as the top-k list alone needs, or more if the
+// concatenation would put more than 768 entries (12 tiles) in one split. The
+// concatenated tiles are spread evenly over them; with k2 = 0 this is the
+// one-split-per-512-entries rule.
 inline int num_splits_total(int k, int k2) {
-  return num_splits_for_k(k) + (k2 > 0 ? num_splits_for_k(k2) : 0);
+  const int a = num_splits_for_k(k);
+  const int b = (k + k2 + 767) / 768;
+  return a > b ? a : b;
 }
 
 struct AttnArgs {

@@ -226,6 +226,22 @@ def mtp_case(name, seq_lens, next_n, H, k, kv_dtype="bf16", seed=5, score_mode="
                 meta={"seq_lens": seq_lens, "next_n": next_n, "seed": seed, "stride": stride})
 
 
+def window_case(win_lens, W, kv_dtype="bf16", seed=7, device="cpu"):
+    """A sliding-window pool: row b's window context has win_lens[b]
+    positions and its index list holds the last min(W, win_lens[b]) of them,
+    padded with -1 to W. Returns (pages, block_table, idx [B, W], lens [B])."""
+    win_lens = [int(n) for n in win_lens]
+    g = _gen(seed, device)
+    bt, num_pages = _block_table([max(1, n) for n in win_lens], g, device)
+    pages = _kv_pool(num_pages, kv_dtype, g, device)
+    idx = torch.full((len(win_lens), W), -1, dtype=torch.int32)
+    for b, n in enumerate(win_lens):
+        m = min(W, n)
+        idx[b, :m] = torch.arange(n - m, n, dtype=torch.int32)
+    lens = torch.tensor(win_lens, dtype=torch.int32)
+    return pages, bt, idx.to(device), lens.to(device)
+
+
 def _uniform_ints(lo, hi, n, seed):
     g = torch.Generator().manual_seed(int(seed) + 1000003)
     return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
@@ -241,6 +257,9 @@ WORKLOADS = {
                            scores="normal", seed=2, stride=131072),
     "chunked_prefill": dict(kind="prefill", T=4096, H=128, ctx=65536, first_pos=61440, k=2048,
                             kv="bf16", scores="normal", seed=3),
+    # TP2 decode plus a 128-entry sliding window (second pool) and per-head sinks.
+    "tp2_decode_swa": dict(kind="decode_swa", B=32, H=64, ctx=(4096, 32768), k=2048, kv="bf16",
+                           scores="normal", seed=6, stride=32768, swa_width=128),
     # MTP4 decode: one target and four draft tokens per request.
     "tp2_mtp4_decode": dict(kind="mtp", B=32, next_n=5, H=64, ctx=(4096, 32768), k=2048,
                             kv="bf16", scores="normal", seed=5, stride=32768),
