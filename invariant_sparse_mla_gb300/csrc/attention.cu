@@ -212,8 +212,6 @@ struct KParams {
 
 template <int HG, bool FP8>
 __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kernel(const KParams p) {
-  pdl_wait();
-  pdl_trigger();
   using LY = Layout<HG>;
   using RL = Roles<FP8>;
   constexpr int RW = RL::kRowsPerWarp, TG = RL::kTileGroups;
@@ -241,6 +239,43 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   const int split = (int)(bid % p.num_splits);
   const int64_t row = bid / p.num_splits;
 
+  // ---- set-up that reads no global memory, done while the previous kernel
+  // of the stream may still run: thread 0 sets up the barriers, one warp
+  // allocates TMEM, and the loaders ask L2 for this CTA's Q tile and (for
+  // decode) its block-table row. L2 is where every write lands, so a line
+  // requested before the previous kernel wrote it is never seen stale.
+  if (tid == 0) {
+    *neff_s = 0;
+    for (int i = 0; i < kNumBars; ++i) {
+      // q_full, kv_full and p_full: one arrival per loader / softmax
+      // thread; s_full: one tcgen05.commit from each QK issuer; the rest:
+      // one tcgen05.commit.
+      uint32_t count = 1u;
+      if (i == kPFull || i == kPFull + 1) count = 128u;
+      if (i == kQFull || (i >= kKvFull && i < kKvFull + kStages)) count = RL::kLoaderThreads;
+      if (i == kSFull || i == kSFull + 1) count = 2u;
+      mbar_init(&bars[i], count);
+    }
+    mbar_fence_init();
+  }
+  if (warp == RL::kQkA) {
+    tmem_alloc(tmem_slot, LY::kTmemCols);
+    tmem_relinquish();
+  }
+  if (producer) {
+    const char* qb = reinterpret_cast<const char*>(p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD);
+    for (int off = (tid - 128) * 128; off < HG * kRowBytesBf16; off += RL::kLoaderThreads * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
+    if (p.row_req == nullptr) {
+      const char* bb = reinterpret_cast<const char*>(p.block_table + row * p.bt_stride);
+      for (int64_t off = (int64_t)(tid - 128) * 128; off < p.bt_stride * 4;
+           off += RL::kLoaderThreads * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(bb + off));
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+
   int64_t bt_row = row;
   bool row_ok = true;
   if (p.row_req != nullptr) {
@@ -266,27 +301,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
 
   // ---- prologue (one block-wide barrier): producers start the Q copies,
-  // read their idx entries and resolve pages; thread 0 sets up the
-  // barriers; warp 8 allocates TMEM.
-  if (tid == 0) {
-    *neff_s = 0;
-    for (int i = 0; i < kNumBars; ++i) {
-      // q_full, kv_full and p_full: one arrival per loader / softmax
-      // thread; s_full: one tcgen05.commit from each QK issuer; the rest:
-      // one tcgen05.commit.
-      uint32_t count = 1u;
-      if (i == kPFull || i == kPFull + 1) count = 128u;
-      if (i == kQFull || (i >= kKvFull && i < kKvFull + kStages)) count = RL::kLoaderThreads;
-      if (i == kSFull || i == kSFull + 1) count = 2u;
-      mbar_init(&bars[i], count);
-    }
-    mbar_fence_init();
-  }
-  if (warp == RL::kQkA) {
-    tmem_alloc(tmem_slot, LY::kTmemCols);
-    tmem_relinquish();
-  }
-  __syncthreads();   // neff_s = 0 is visible before any atomicMax below
+  // read their idx entries and resolve pages.
+  __syncthreads();   // barriers, TMEM and neff_s = 0 are visible before use
   // KV row (page * 64 + slot) of each owned entry, -1 = skip: slot i is
   // tile lgroup + TG i, row RW pw + lrow.
   int grow[4] = {-1, -1, -1, -1};
