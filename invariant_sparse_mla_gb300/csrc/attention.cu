@@ -67,6 +67,11 @@ constexpr int kOCol = 4 * kSCols;                     // first TMEM column of O^
 constexpr int kMaxSplitTiles = 12;                    // tiles one split may hold
 constexpr int kQkSplitAtom = 5;                       // QK column blocks [0,5) -> S_a, [5,9) -> S_b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
+// P(t) is written over the rope column block of tile t's own stage: QK(t) is
+// its only reader and has completed once S(t) is ready, PV(t) never reads it,
+// and the stage is refilled only after PV(t). So P is double-buffered with
+// the stages at no cost in shared memory.
+constexpr int kPAtom = 8 * kAtomStride;
 
 // Warp roles. Warps 0-3 run the softmax; warps 4-11 load; then come one QK
 // issuer, the PV issuer and the second QK issuer. Loader warp pw fills rows
@@ -99,9 +104,7 @@ struct Layout {
   static constexpr int kQBytes = HG * kRowBytesBf16;
   static constexpr int kQ = 0;
   static constexpr int kKV = kQ + kQBytes;                    // kStages x kStageBytes
-  static constexpr int kP = kKV + kStages * kStageBytes;      // HG rows x 128 B (64 entries)
-  static constexpr int kPBytes = HG * 128;
-  static constexpr int kBars = kP + kPBytes;                  // 16 x u64
+  static constexpr int kBars = kKV + kStages * kStageBytes;   // 16 x u64
   static constexpr int kMask = kBars + 16 * 8;                // kMaxSplitTiles x u64
   static constexpr int kAlpha = kMask + kMaxSplitTiles * 8;   // 2 x 64 floats
   static constexpr int kTmemSlot = kAlpha + 2 * 64 * 4;       // u32
@@ -117,12 +120,11 @@ struct Layout {
 enum Bar {
   kQFull = 0,      // loader threads -> QK issuers (Q landed)
   kKvFull = 1,     // 2: loader threads -> QK issuers (tile landed)
-  kKvEmpty = 3,    // 2: PV issuer commit -> loaders (stage free)
+  kKvEmpty = 3,    // 2: PV issuer commit -> loaders (stage free), softmax (O^T holds the tile)
   kSFull = 5,      // 2: both QK issuers' commits -> softmax (S ready)
   kPFull = 7,      // 2: softmax threads -> PV issuer, QK issuers (P written, S read)
-  kPvDone = 9,     // PV issuer commit -> softmax (PV of a tile done)
-  kMmaDone = 10,   // 3: each issuer's final drain
-  kNumBars = 13
+  kMmaDone = 9,    // 3: each issuer's final drain
+  kNumBars = 12
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -300,20 +302,13 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   auto tile_kv = [&](int t) { return u0 + t >= T1 ? p.kv2 : p.kv; };
   const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
 
-  // ---- prologue (one block-wide barrier): producers start the Q copies,
-  // read their idx entries and resolve pages.
+  // ---- prologue (one block-wide barrier): producers read their idx
+  // entries, resolve pages and start the tile 0 and Q copies.
   __syncthreads();   // barriers, TMEM and neff_s = 0 are visible before use
   // KV row (page * 64 + slot) of each owned entry, -1 = skip: slot i is
   // tile lgroup + TG i, row RW pw + lrow.
   int grow[4] = {-1, -1, -1, -1};
   if (producer) {
-    const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
-    const int ptid = tid - 128;
-    for (int c = ptid; c < HG * kChunks; c += RL::kLoaderThreads) {
-      const int h = c / kChunks, ch = c - h * kChunks;
-      cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
-    }
-    cp_async_commit();
     int pos[4] = {-1, -1, -1, -1};
     bool sec[4] = {false, false, false, false};   // slot's tile is in the second list
     int last = 0;
@@ -369,9 +364,12 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
         }
       }
     }
-    // Start tile 0 (stage 0) and stream tiles 2 and 3 into L2 right away,
-    // before the block-wide barrier. Entries that are not valid copy zeros,
-    // so this is harmless when the split turns out to be empty.
+    // Start tile 0 (stage 0), then Q, and stream tiles 2 and 3 into L2
+    // right away, before the block-wide barrier. The entry lookups go first
+    // because tile 0 waits on them and then on HBM, while Q was requested
+    // into L2 before the wait on the previous kernel; its copies, issued
+    // behind tile 0's, land about as early. Entries that are not valid copy
+    // zeros, so this is harmless when the split turns out to be empty.
     {
       const uint32_t stage_base = sbase + LY::kKV;
       const int row_bytes = FP8 ? kRowBytesFp8 : kRowBytesBf16;
@@ -391,6 +389,13 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
         }
         cp_async_commit();
       }
+      const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
+      for (int c = tid - 128; c < HG * kChunks; c += RL::kLoaderThreads) {
+        const int h = c / kChunks, ch = c - h * kChunks;
+        cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
+      }
+      cp_async_commit();
+      if constexpr (!FP8) cp_async_mbar_arrive_noinc(&bars[kQFull]);
 #pragma unroll
       for (int u = 2; u < 4; ++u) {   // tiles 2 and 3
         if (u < ntiles && lgroup == u % TG) {
@@ -421,9 +426,12 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     }
   } else if (producer) {
     // ------------------------------------------------------------ producers
-    // All loader warps fill each tile in turn (RW rows each) into stage t & 1,
-    // wait for their own copies (or stores) to land, fence them for the
-    // tensor core and arrive. Q shares the first tile's wait. Shared memory
+    // All loader warps fill each tile in turn (RW rows each) into stage t & 1.
+    // bf16: the copies arrive on the tile's barrier by themselves when they
+    // land (cp.async.mbarrier.arrive), so a loader moves on to the next stage
+    // as soon as it is free and up to two tiles are in flight; the tensor-core
+    // issuers fence the landed tiles for the async proxy. FP8: the loaders
+    // dequantise through registers, store, fence and arrive. Shared memory
     // holds only two tiles, so L2 serves as the deeper stages: while tile t is
     // copied, the rows of tile t + 3 are streamed into L2 with bulk
     // prefetches (tiles 2 and 3 at the start), in tile order, so each tile's
@@ -465,8 +473,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
           }
         }
         cp_async_commit();
+        cp_async_mbar_arrive_noinc(&bars[kKvFull + stage]);
         prefetch_ahead(t, kRowBytesBf16);
-        cp_async_wait_all();
       } else {
         prefetch_ahead(t, kRowBytesFp8);
         if (t == 0) cp_async_wait_all();   // Q
@@ -506,9 +514,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
           }
         }
       }
-      fence_proxy_async_smem();
-      if (t == 0) mbar_arrive(&bars[kQFull]);
-      mbar_arrive(&bars[kKvFull + stage]);
+      if constexpr (FP8) {
+        fence_proxy_async_smem();
+        if (t == 0) mbar_arrive(&bars[kQFull]);
+        mbar_arrive(&bars[kKvFull + stage]);
+      }
     }
     cp_async_wait_all();
   } else if (warp == RL::kQkA || warp == RL::kQkB) {
@@ -532,6 +542,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
           failed = true;
           break;
         }
+        // The tile (and Q) landed through cp.async, a generic-proxy write:
+        // order it before the tensor core's async-proxy reads.
+        fence_proxy_async_smem();
         tc_fence_after();
         const uint64_t b0 = kv_desc0 + (uint64_t)((sb * kStageBytes) >> 4);
         const uint32_t d = tmem + s_col + sb * kSCols;
@@ -558,7 +571,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     // overwrite P and rescale O^T.
     if (lane == 0) {
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, HG, 1, 0);
-      const uint64_t p_desc = make_sw128_desc(sbase + LY::kP, 16, 1024);
+      const uint64_t p_desc0 = make_sw128_desc(sbase + LY::kKV + kPAtom, 16, 1024);
       const uint64_t v_desc0 = make_sw128_desc(sbase + LY::kKV, kAtomStride, 1024);
       for (int t = 0; t < n_eff && !failed; ++t) {
         const int sb = t & 1;
@@ -566,18 +579,19 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
           failed = true;
           break;
         }
+        fence_proxy_async_smem();   // V landed through cp.async
         tc_fence_after();
         const uint64_t a0 = v_desc0 + (uint64_t)((sb * kStageBytes) >> 4);
+        const uint64_t p0 = p_desc0 + (uint64_t)((sb * kStageBytes) >> 4);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             mma_bf16_ss(tmem + kOCol + b * HG, a0 + (((2 * b * kAtomStride) + kk * 2048) >> 4),
-                        p_desc + ((kk * 32) >> 4), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                        p0 + ((kk * 32) >> 4), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
           }
         }
         mma_commit(&bars[kKvEmpty + sb]);
-        mma_commit(&bars[kPvDone]);
       }
       mma_commit(&bars[kMmaDone + 1]);
       mbar_wait(&bars[kMmaDone + 1], 0);
@@ -596,7 +610,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     const bool active = h < HG;
     const bool warp_has_heads = warp * 16 < HG;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint8_t* prow = smem + LY::kP + (h >> 3) * 1024 + (h & 7) * 128;
+    const uint32_t prow = sbase + LY::kKV + kPAtom + (h >> 3) * 1024 + (h & 7) * 128;
     float m = -INFINITY, l = 0.0f;   // l: this half's share of the row sum
     float s[32];
     // The four softmax warps meet at named barriers (ids 1-2), so every
@@ -630,8 +644,6 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
           }
           if (active && half == 0) alpha_s[sb * 64 + h] = a;
         }
-        // P(t) overwrites P(t-1) and O^T may be rescaled: PV(t-1) must be done.
-        if (t > 0) ok = mbar_wait(&bars[kPvDone], (t - 1) & 1);
       }
       if (named_bar_or(1, 128, !ok)) {
         failed = true;
@@ -655,11 +667,21 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
             w[i] = *reinterpret_cast<const uint32_t*>(&pb);
           }
           const int c8 = 4 * half + c4;   // 16-byte chunk of the 128-byte P row
-          st_shared_v4(smem_u32(prow) + ((c8 ^ (h & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+          st_shared_v4(prow + sb * kStageBytes + ((c8 ^ (h & 7)) << 4),
+                       make_uint4(w[0], w[1], w[2], w[3]));
         }
         l += lsum;
       }
       if (any) {
+        // O^T must hold PV(t-1) before it is rescaled. Tile t was loaded after
+        // PV(t-2) completed, so the stage barrier of PV(t-1) is at most one
+        // phase from it and its parity test is exact.
+        const bool pv_ok = mbar_wait(&bars[kKvEmpty + ((t - 1) & 1)], ((t - 1) >> 1) & 1);
+        if (named_bar_or(1, 128, !pv_ok)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
         // O^T lanes are dv rows; columns are heads. Scale column h by alpha[h].
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
@@ -679,7 +701,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       tc_fence_before();
       mbar_arrive(&bars[kPFull + sb]);
     }
-    if (!failed && !mbar_wait(&bars[kPvDone], (n_eff - 1) & 1)) failed = true;
+    if (!failed && !mbar_wait(&bars[kKvEmpty + ((n_eff - 1) & 1)], ((n_eff - 1) >> 1) & 1))
+      failed = true;
     if (!failed) {
       tc_fence_after();
       // Epilogue: partial O (unnormalised, relative to m), m and l.

@@ -84,6 +84,14 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// Arrives once on `bar` when every cp.async this thread issued so far has
+// landed; the thread itself does not wait. The arrival is one of the counts
+// the barrier was initialised with (no pending count is added).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (the tensor core reads its operands through the async
 // proxy).
