@@ -118,7 +118,7 @@ struct Layout {
 // for a phase that cannot be overtaken by the next one, so the parity test
 // is unambiguous.
 enum Bar {
-  kQFull = 0,      // loader threads -> QK issuers (Q landed)
+  kQFull = 0,      // softmax threads' Q copies -> QK issuers (Q landed)
   kKvFull = 1,     // 2: loader threads -> QK issuers (tile landed)
   kKvEmpty = 3,    // 2: PV issuer commit -> loaders (stage free), softmax (O^T holds the tile)
   kSFull = 5,      // 2: both QK issuers' commits -> softmax (S ready)
@@ -177,6 +177,24 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 
 // Starts an asynchronous copy of `bytes` (a multiple of 16, 16-byte aligned
 // source) from global memory into L2, without waiting for it.
+// Requests every 128-byte line of [base, base + bytes) into L2 (or into this
+// SM's L1), thread `first` of `step` threads taking every step-th line. A
+// line that holds a byte of the range lies in a mapped page, so no request
+// leaves the range's pages.
+template <bool kL1>
+__device__ __forceinline__ void prefetch_lines(const void* base, int64_t bytes, int first,
+                                               int step) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+  const uintptr_t end = b + (uintptr_t)bytes;
+  for (uintptr_t a = (b & ~uintptr_t(127)) + (uintptr_t)first * 128u; a < end;
+       a += (uintptr_t)step * 128u) {
+    if constexpr (kL1)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a) : "memory");
+    else
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
+  }
+}
+
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
@@ -230,7 +248,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // The loader warps load Q and every KV tile together (see Roles).
+  // The loader warps load every KV tile together (see Roles); the softmax
+  // warps copy Q.
   const bool producer = warp >= 4 && warp < 4 + RL::kLoaderWarps;
   const int pw = warp - 4;
   const int lgroup = lane / RW, lrow = lane % RW;   // tile group and row of this lane
@@ -254,7 +273,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       // one tcgen05.commit.
       uint32_t count = 1u;
       if (i == kPFull || i == kPFull + 1) count = 128u;
-      if (i == kQFull || (i >= kKvFull && i < kKvFull + kStages)) count = RL::kLoaderThreads;
+      if (i == kQFull) count = 128u;
+      if (i >= kKvFull && i < kKvFull + kStages) count = RL::kLoaderThreads;
       if (i == kSFull || i == kSFull + 1) count = 2u;
       mbar_init(&bars[i], count);
     }
@@ -265,15 +285,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     tmem_relinquish();
   }
   if (producer) {
-    const char* qb = reinterpret_cast<const char*>(p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD);
-    for (int off = (tid - 128) * 128; off < HG * kRowBytesBf16; off += RL::kLoaderThreads * 128)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
-    if (p.row_req == nullptr) {
-      const char* bb = reinterpret_cast<const char*>(p.block_table + row * p.bt_stride);
-      for (int64_t off = (int64_t)(tid - 128) * 128; off < p.bt_stride * 4;
-           off += RL::kLoaderThreads * 128)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(bb + off));
-    }
+    prefetch_lines<false>(p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD,
+                          HG * kRowBytesBf16, tid - 128, RL::kLoaderThreads);
+    if (p.row_req == nullptr)
+      prefetch_lines<false>(p.block_table + row * p.bt_stride, p.bt_stride * 4, tid - 128,
+                            RL::kLoaderThreads);
   }
   pdl_wait();
   pdl_trigger();
@@ -303,11 +319,44 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   const int64_t part_base = ((int64_t)split * p.R + row) * p.H + (int64_t)hg * HG;
 
   // ---- prologue (one block-wide barrier): producers read their idx
-  // entries, resolve pages and start the tile 0 and Q copies.
+  // entries, resolve pages and start the tile 0 and 1 copies; the softmax
+  // warps copy Q.
   __syncthreads();   // barriers, TMEM and neff_s = 0 are visible before use
+  if (tid < 128) {
+    // The softmax warps have nothing to do until the first S: they copy Q
+    // (requested into L2 before the wait) while the loaders look up entries,
+    // so Q's copies never queue ahead of a KV tile's.
+    const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
+    for (int c = tid; c < HG * kChunks; c += 128) {
+      const int h = c / kChunks, ch = c - h * kChunks;
+      cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
+    }
+    cp_async_commit();
+    cp_async_mbar_arrive_noinc(&bars[kQFull]);
+  }
   // KV row (page * 64 + slot) of each owned entry, -1 = skip: slot i is
   // tile lgroup + TG i, row RW pw + lrow.
   int grow[4] = {-1, -1, -1, -1};
+  // bf16 pools: loader warp pw copies rows RW pw .. RW pw + RW - 1 of tile t
+  // into the stage at stage_base, 16-byte cp.async into the 128-byte
+  // swizzled layout; entries that are not valid copy zeros.
+  auto copy_tile_bf16 = [&](int t, uint32_t stage_base) {
+    const int gi = slot_row(grow, t / TG);
+    const int src_lane0 = (t % TG) * RW;
+#pragma unroll 4
+    for (int rr = 0; rr < RW; ++rr) {
+      const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + rr);
+      const uint8_t* src = tile_kv(t) + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
+      const uint32_t nbytes = g >= 0 ? 16u : 0u;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int c = lane + 32 * j;
+        if (c < kChunks)
+          cp_async_16(stage_base + swz_off(RW * pw + rr, c, kAtomStride), src + c * 16, nbytes);
+      }
+    }
+    cp_async_commit();
+  };
   if (producer) {
     int pos[4] = {-1, -1, -1, -1};
     bool sec[4] = {false, false, false, false};   // slot's tile is in the second list
@@ -321,8 +370,21 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
         pos[i] = sec[i] ? idx_row2[(u - T1) * kTile + RW * pw + lrow]
                         : idx_row1[u * kTile + RW * pw + lrow];
       }
-      if (pos[i] != -1) last = t + 1;
     }
+    // While the entries are in flight, bring the block-table row(s) into
+    // this SM's L1 (after the wait on the previous kernel, so nothing stale
+    // is cached): the page lookups below then hit L1 instead of making a
+    // second round trip to L2.
+    if (row_ok) {
+      prefetch_lines<true>(p.block_table + bt_row * p.bt_stride, p.bt_stride * 4, tid - 128,
+                           RL::kLoaderThreads);
+      if (p.k2 > 0)
+        prefetch_lines<true>(p.block_table2 + bt_row * p.bt_stride2, p.bt_stride2 * 4,
+                             tid - 128, RL::kLoaderThreads);
+    }
+#pragma unroll
+    for (int i = 0; i < RL::kSlots; ++i)
+      if (pos[i] != -1) last = lgroup + TG * i + 1;
     // All block-table reads go out before any is used: one round trip.
     int64_t page[4];
 #pragma unroll
@@ -364,38 +426,23 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
         }
       }
     }
-    // Start tile 0 (stage 0), then Q, and stream tiles 2 and 3 into L2
-    // right away, before the block-wide barrier. The entry lookups go first
-    // because tile 0 waits on them and then on HBM, while Q was requested
-    // into L2 before the wait on the previous kernel; its copies, issued
-    // behind tile 0's, land about as early. Entries that are not valid copy
-    // zeros, so this is harmless when the split turns out to be empty.
+    // Start tile 0 (stage 0) and tile 1 (stage 1), and stream tiles 2 and 3
+    // into L2 right away, before the block-wide barrier, in the order they
+    // are needed: every CTA starts at once, so requests issued later queue
+    // behind earlier ones at HBM. Entries that are not valid copy zeros, so
+    // this is harmless when the split turns out to be short.
     {
-      const uint32_t stage_base = sbase + LY::kKV;
       const int row_bytes = FP8 ? kRowBytesFp8 : kRowBytesBf16;
+      // Each arrival tracks every earlier copy of the thread, so tile 0
+      // signals its barrier before tile 1 is issued.
       if constexpr (!FP8) {
-#pragma unroll 4
-        for (int rr = 0; rr < RW; ++rr) {   // tile 0: lanes 0 .. RW - 1, slot 0
-          const int64_t g = __shfl_sync(0xffffffffu, grow[0], rr);
-          const uint8_t* src = tile_kv(0) + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
-          const uint32_t nbytes = g >= 0 ? 16u : 0u;
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            const int c = lane + 32 * j;
-            if (c < kChunks)
-              cp_async_16(stage_base + swz_off(RW * pw + rr, c, kAtomStride), src + c * 16,
-                          nbytes);
-          }
-        }
-        cp_async_commit();
+        copy_tile_bf16(0, sbase + LY::kKV);
+        cp_async_mbar_arrive_noinc(&bars[kKvFull]);
       }
-      const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
-      for (int c = tid - 128; c < HG * kChunks; c += RL::kLoaderThreads) {
-        const int h = c / kChunks, ch = c - h * kChunks;
-        cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
+      if constexpr (!FP8) {
+        copy_tile_bf16(1, sbase + LY::kKV + kStageBytes);
+        cp_async_mbar_arrive_noinc(&bars[kKvFull + 1]);
       }
-      cp_async_commit();
-      if constexpr (!FP8) cp_async_mbar_arrive_noinc(&bars[kQFull]);
 #pragma unroll
       for (int u = 2; u < 4; ++u) {   // tiles 2 and 3
         if (u < ntiles && lgroup == u % TG) {
@@ -419,7 +466,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   bool failed = false;
   if (n_eff == 0) {
     // Nothing to attend to in this split: an empty partial.
-    if (producer) cp_async_wait_all();  // Q copies must land before the CTA exits
+    if (producer || tid < 128) cp_async_wait_all();  // copies land before the CTA exits
     if (tid < HG) {
       p.part_m[part_base + tid] = -INFINITY;
       p.part_l[part_base + tid] = 0.0f;
@@ -456,28 +503,16 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
         failed = true;
         break;
       }
-      const int gi = slot_row(grow, t / TG);
-      const int src_lane0 = (t % TG) * RW;
       if constexpr (!FP8) {
-#pragma unroll 4
-        for (int rr = 0; rr < RW && t > 0; ++rr) {   // tile 0 was issued in the prologue
-          const int64_t g = __shfl_sync(0xffffffffu, gi, src_lane0 + rr);
-          const uint8_t* src = tile_kv(t) + (g >= 0 ? g : 0) * (int64_t)kRowBytesBf16;
-          const uint32_t nbytes = g >= 0 ? 16u : 0u;
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            const int c = lane + 32 * j;
-            if (c < kChunks)
-              cp_async_16(stage_base + swz_off(RW * pw + rr, c, kAtomStride), src + c * 16,
-                          nbytes);
-          }
+        if (t >= 2) {   // tiles 0 and 1 went out in the prologue
+          copy_tile_bf16(t, stage_base);
+          cp_async_mbar_arrive_noinc(&bars[kKvFull + stage]);
         }
-        cp_async_commit();
-        cp_async_mbar_arrive_noinc(&bars[kKvFull + stage]);
         prefetch_ahead(t, kRowBytesBf16);
       } else {
+        const int gi = slot_row(grow, t / TG);
+        const int src_lane0 = (t % TG) * RW;
         prefetch_ahead(t, kRowBytesFp8);
-        if (t == 0) cp_async_wait_all();   // Q
 #pragma unroll 1
         for (int r0 = 0; r0 < RW; r0 += 8) {
           uint2 codes[8][2];
@@ -516,7 +551,6 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       }
       if constexpr (FP8) {
         fence_proxy_async_smem();
-        if (t == 0) mbar_arrive(&bars[kQFull]);
         mbar_arrive(&bars[kKvFull + stage]);
       }
     }
@@ -730,6 +764,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     }
   }
 
+  if (tid < 128) cp_async_wait_all();   // Q copies, on every path
   if (failed && p.err != nullptr) atomicOr(p.err, kErrTimeout);
   tc_fence_before();
   __syncthreads();
