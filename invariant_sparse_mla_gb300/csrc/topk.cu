@@ -433,21 +433,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_smem_kernel(
   row_pick<kRowBins>(sm.hist, take, sm.wsum, sm.pick, P, cnt, take);
 
   // Thread t's positions [32t, 32t + 32): 8 granules, read in a lane-rotated
-  // order so that the warp's 16-byte reads hit distinct banks.
+  // order so that the warp's 16-byte reads hit distinct banks. A key's 12-bit
+  // prefix is above P iff the key is at least (P + 1) << 20, and equal to P
+  // iff it is at least P << 20 and not above; each granule's four bits are
+  // gathered first and placed with one shift.
   const int base = 32 * tid;
   uint32_t sel = 0u, eqw = 0u;
   if (base < L) {
+    const uint32_t lo = P << 20;
+    const bool top = P == kRowBins - 1u;   // no prefix lies above the top bin
+    const uint32_t hi = top ? 0u : (P + 1u) << 20;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int cc = (c + lane) & 7;
       const uint4 w = key4[8 * tid + cc];
-      const uint32_t kk[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t pre = kk[q] >> 20;
-        sel |= (pre > P ? 1u : 0u) << (4 * cc + q);
-        eqw |= (pre == P ? 1u : 0u) << (4 * cc + q);
-      }
+      uint32_t gs = (uint32_t)(w.x >= hi) | ((uint32_t)(w.y >= hi) << 1) |
+                    ((uint32_t)(w.z >= hi) << 2) | ((uint32_t)(w.w >= hi) << 3);
+      if (top) gs = 0u;
+      const uint32_t ge = (uint32_t)(w.x >= lo) | ((uint32_t)(w.y >= lo) << 1) |
+                          ((uint32_t)(w.z >= lo) << 2) | ((uint32_t)(w.w >= lo) << 3);
+      sel |= gs << (4 * cc);
+      eqw |= (ge & ~gs) << (4 * cc);
     }
     if (L - base < 32) {
       const uint32_t valid = (1u << (L - base)) - 1u;
