@@ -16,7 +16,10 @@ around K steps replayed from a CUDA graph, inputs resident in HBM. Four
 independent input sets rotate so the gathered KV (4 x 75.5 MB) exceeds the
 129 MB L2 between reuses. `e2e` repeats the step through the public API with
 pinned host buffers: the step's inputs are copied host->device, and out, lse
-and idx are read back, inside the timed region. Under torchrun every rank
+and idx are read back, inside the timed region, with four steps in flight on
+four streams (copies run at about 200 GB/s, so one step's 9 MB of transfers
+take about as long as its kernels). Independent steps' kernels then overlap
+too, so `e2e` can exceed the single-stream `value`. Under torchrun every rank
 runs its own batch (rows are independent: weak scaling, no collective on the
 data path).
 
@@ -64,6 +67,7 @@ WORKLOAD_DESCS = {
 }
 METRIC = "sparse-MLA decode tokens/s and top-k rows/s on 1 GB300; % of roofline"
 N_SETS = 4
+E2E_SLOTS = 4   # steps in flight end to end: 2 -> 500 K, 3 -> 708 K, 4 -> 813 K tokens/s measured
 HBM_CONTRACT_GBS = 8000.0
 
 
@@ -75,6 +79,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-slots", type=int, default=E2E_SLOTS,
+                    help="steps in flight in the end-to-end loop (each its own stream and buffers)")
     ap.add_argument("--sets", type=int, default=N_SETS,
                     help="rotating input sets (profiling runs use 1 to stay small)")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESCS), default=WORKLOAD,
@@ -368,6 +374,7 @@ def run_ours(args, rank, world, local):
     # End to end through the public API with pinned host buffers.
     e2e = None if (args.no_e2e or w["kind"] != "decode") else run_e2e(ds, sets, stream, dev,
                                            steps_e2e=max(20, min(400, args.steps // 50)),
+                                           n_slots=args.e2e_slots,
                                            world=world)
 
     hbm, tflops, peak_kind = load_peaks()
@@ -432,16 +439,16 @@ def run_ours(args, rank, world, local):
     return line
 
 
-def run_e2e(ds, sets, stream, dev, steps_e2e, world):
+def run_e2e(ds, sets, stream, dev, steps_e2e, world, n_slots=E2E_SLOTS):
     """Host -> device inputs, the two calls, device -> host results, every step.
 
     A serving loop: each step's inputs (scores, row bounds, q, block table,
     lengths) are packed in one pinned host buffer and copied with one H2D copy;
     idx, out and lse land in one device buffer read back with one D2H copy.
-    Two steps are in flight (ping-pong slots, each on its own stream), so one
-    step's transfers overlap the other's kernels. Before a slot is reused the
-    host waits for that slot's previous download, so every step's result is
-    on the host within the timed region.
+    `n_slots` steps are in flight (slots used in turn, each on its own stream),
+    so one step's transfers overlap another's kernels. Before a slot is reused
+    the host waits for that slot's previous download, so every step's result
+    is on the host within the timed region.
     """
     import torch
     in_names = ("scores", "row_starts", "row_ends", "q", "block_table", "lens")
@@ -471,7 +478,7 @@ def run_e2e(ds, sets, stream, dev, steps_e2e, world):
             hv[n].copy_(getattr(c, n).cpu())
         host_in.append(hb)
     slots = []
-    for _ in range(2):
+    for _ in range(n_slots):
         din = torch.empty(max(b for b, _ in lay_in), dtype=torch.uint8, device=dev)
         dout = torch.empty(max(b for b, _ in lay_out), dtype=torch.uint8, device=dev)
         hout = torch.empty(dout.numel(), dtype=torch.uint8).pin_memory()
@@ -485,9 +492,9 @@ def run_e2e(ds, sets, stream, dev, steps_e2e, world):
     # Each (slot, input set) step is captured once as a CUDA graph of the
     # public calls: upload, top-k, decode, download (the calls allocate
     # nothing and never synchronise, so they capture as they are). Slot j
-    # replays on its own stream, so step i + 1's upload and step i - 1's
-    # download overlap step i's kernels.
-    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    # replays on its own stream, so the uploads and downloads of the steps in
+    # flight overlap each other's kernels.
+    streams = [torch.cuda.Stream(dev) for _ in range(n_slots)]
 
     def record(j, sl):
         c, hin = sets[j], host_in[j]
@@ -515,7 +522,7 @@ def run_e2e(ds, sets, stream, dev, steps_e2e, world):
             sl["graphs"].append(g)
 
     def one(i):
-        si = i % 2
+        si = i % n_slots
         sl = slots[si]
         if sl["used"]:
             sl["out_done"].synchronize()   # the host has step i - 2's result
@@ -543,8 +550,8 @@ def run_e2e(ds, sets, stream, dev, steps_e2e, world):
     return {"value": round(world * R * steps_e2e / secs, 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps_e2e,
             "timing": "host wall clock from the first upload to the last result on the host",
-            "pipelining": "two steps in flight; each step is one CUDA graph of the public calls "
-                          "(upload, top-k, decode, download), the two slots on two streams",
+            "pipelining": f"{n_slots} steps in flight; each step is one CUDA graph of the public "
+                          "calls (upload, top-k, decode, download), each slot on its own stream",
             "kv_cache": "resident on the device (serving state, not a per-step input)"}
 
 
