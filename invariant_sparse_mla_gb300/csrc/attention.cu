@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
         copy_tile_bf16(0, sbase + LY::kKV);
         cp_async_mbar_arrive_noinc(&bars[kKvFull]);
       }
-      if constexpr (!FP8) {
+      if (!FP8 && ntiles > 1) {   // a one-tile split has no tile 1 (nor its pool)
         copy_tile_bf16(1, sbase + LY::kKV + kStageBytes);
         cp_async_mbar_arrive_noinc(&bars[kKvFull + 1]);
       }
