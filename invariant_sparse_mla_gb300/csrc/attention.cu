@@ -262,9 +262,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 
   // ---- set-up that reads no global memory, done while the previous kernel
   // of the stream may still run: thread 0 sets up the barriers, one warp
-  // allocates TMEM, and the loaders ask L2 for this CTA's Q tile and (for
-  // decode) its block-table row. L2 is where every write lands, so a line
-  // requested before the previous kernel wrote it is never seen stale.
+  // allocates TMEM, and the loaders ask L2 for this CTA's Q tile, (for
+  // decode) its block-table row, its row length and its top-k entries. L2 is
+  // where every write lands, so a line requested before the previous kernel
+  // wrote it is never seen stale.
   if (tid == 0) {
     *neff_s = 0;
     for (int i = 0; i < kNumBars; ++i) {
@@ -284,12 +285,29 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     tmem_alloc(tmem_slot, LY::kTmemCols);
     tmem_relinquish();
   }
+  // The concatenated entry list [top-k list || second list] in 64-entry
+  // tiles: tile u < T1 holds top-k entries 64u .. 64u + 63 (main pool), tile
+  // u >= T1 entries 64(u - T1) .. of the second list (its own pool). Split s
+  // owns tiles [floor(s T / S), floor((s + 1) T / S)): a function of k and
+  // the second list's width alone, never of the batch.
+  const int T1 = p.k / kTile;
+  const int T = T1 + p.k2 / kTile;
+  const int u0 = (int)((int64_t)split * T / p.num_splits);
+  const int ntiles = (int)((int64_t)(split + 1) * T / p.num_splits) - u0;
   if (producer) {
     prefetch_lines<false>(p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD,
                           HG * kRowBytesBf16, tid - 128, RL::kLoaderThreads);
     if (p.row_req == nullptr)
       prefetch_lines<false>(p.block_table + row * p.bt_stride, p.bt_stride * 4, tid - 128,
                             RL::kLoaderThreads);
+    // The split's top-k entries, usually written by the kernel still running
+    // ahead of this one: the request warms L2 and this SM's address
+    // translation for the first reads after the wait.
+    const int u_end = min(u0 + ntiles, T1);
+    if (u_end > u0)
+      prefetch_lines<false>(p.idx + row * (int64_t)p.k + u0 * kTile,
+                            (int64_t)(u_end - u0) * kTile * 4, tid - 128, RL::kLoaderThreads);
+    prefetch_lines<false>(p.lens + row, 4, tid - 128, RL::kLoaderThreads);
   }
   pdl_wait();
   pdl_trigger();
@@ -300,15 +318,6 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     bt_row = p.row_req[row];
     row_ok = bt_row >= 0 && bt_row < p.num_bt_rows;
   }
-  // The concatenated entry list [top-k list || second list] in 64-entry
-  // tiles: tile u < T1 holds top-k entries 64u .. 64u + 63 (main pool), tile
-  // u >= T1 entries 64(u - T1) .. of the second list (its own pool). Split s
-  // owns tiles [floor(s T / S), floor((s + 1) T / S)): a function of k and
-  // the second list's width alone, never of the batch.
-  const int T1 = p.k / kTile;
-  const int T = T1 + p.k2 / kTile;
-  const int u0 = (int)((int64_t)split * T / p.num_splits);
-  const int ntiles = (int)((int64_t)(split + 1) * T / p.num_splits) - u0;
   int64_t len1 = p.lens[row], len2 = p.k2 > 0 ? p.lens2[row] : 0;
   if (len1 < 0) len1 = 0;
   if (len2 < 0) len2 = 0;
