@@ -130,12 +130,20 @@ def load_peaks():
 
 
 def kernel_source_sha():
+    """Hash of the kernel sources' code: comments and blank lines are dropped
+    first, so editing a comment does not orphan the committed ncu counters."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "invariant_sparse_mla_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"(?m)^\s*//.*$", "", text)        # whole-line comments
+        text = re.sub(r"(?m)\s+//[^\"\n]*$", "", text)    # trailing comments (no quote after //)
+        code = "\n".join(l.rstrip() for l in text.splitlines() if l.strip())
+        h.update(name.encode())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

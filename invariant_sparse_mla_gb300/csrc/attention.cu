@@ -16,7 +16,8 @@
 //   loader warps        gather 64-entry tiles of 1152-byte bf16 rows into a
 //                       128-byte-swizzled shared-memory tile (FP8 rows are
 //                       dequantised to bf16 on the way), double buffered:
-//                       warps 4-11;
+//                       warps 4-11; bf16 copies arrive on the tile's
+//                       barrier by themselves when they land;
 //   MMA warps           the next three warps; one thread each issues tcgen05
 //                       MMAs (a single thread can issue one MMA per ~54
 //                       cycles, so three issuers keep the tensor pipe fed):
@@ -26,10 +27,11 @@
 //                         PV issuer:  O^T += V^T P^T M=128 (dv block), N=heads, K=64
 //                       The same swizzled tile is the K-major B operand of
 //                       the first and the MN-major A operand of the second.
-//   softmax warps 0-3   read S from TMEM (one head per TMEM lane), keep a
-//                       running max m and sum l per head, write P (bf16) to
-//                       shared memory, and rescale O^T in TMEM only when a
-//                       head's max grows by more than 2^8 (exact: p <= 256
+//   softmax warps 0-3   copy Q in the prologue, then read S from TMEM (one
+//                       head per TMEM lane), keep a running max m and sum l
+//                       per head, write P (bf16) over the rope block of the
+//                       tile's own stage, and rescale O^T in TMEM only when
+//                       a head's max grows by more than 2^8 (exact: p <= 256
 //                       is kept relative to the stored max).
 //
 // The QK MMA has M = 64: for head groups smaller than 64, the A descriptor
@@ -269,9 +271,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   if (tid == 0) {
     *neff_s = 0;
     for (int i = 0; i < kNumBars; ++i) {
-      // q_full, kv_full and p_full: one arrival per loader / softmax
-      // thread; s_full: one tcgen05.commit from each QK issuer; the rest:
-      // one tcgen05.commit.
+      // q_full and p_full: one arrival per softmax thread; kv_full: one per
+      // loader thread; s_full: one tcgen05.commit from each QK issuer; the
+      // rest: one tcgen05.commit.
       uint32_t count = 1u;
       if (i == kPFull || i == kPFull + 1) count = 128u;
       if (i == kQFull) count = 128u;
