@@ -1,0 +1,61 @@
+"""Host-side pieces of bench.py that need no GPU.
+
+The roofline line carries the DRAM traffic of the committed ncu capture only
+while the kernel sources are the ones that capture ran on; the check is a hash
+of the sources' code (comments dropped). These tests pin that rule: a comment
+edit keeps the hash, a code edit changes it, and a record taken on other
+sources is not used.
+"""
+
+import json
+import os
+import shutil
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _copy_csrc(tmp_path):
+    dst = tmp_path / "invariant_sparse_mla_gb300" / "csrc"
+    shutil.copytree(os.path.join(ROOT, "invariant_sparse_mla_gb300", "csrc"), dst)
+    return dst
+
+
+def _sha_at(monkeypatch, root):
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    return bench.kernel_source_sha()
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    csrc = _copy_csrc(tmp_path)
+    base = _sha_at(monkeypatch, tmp_path)
+    f = csrc / "attention.cu"
+    text = f.read_text()
+    f.write_text("// a new leading comment\n/* and a block\n   comment */\n" +
+                 text.replace("constexpr int kStages = 2;",
+                              "constexpr int kStages = 2;   // trailing note"))
+    assert _sha_at(monkeypatch, tmp_path) == base
+    f.write_text(text.replace("constexpr int kStages = 2;", "constexpr int kStages = 3;"))
+    assert _sha_at(monkeypatch, tmp_path) != base
+
+
+def test_traffic_record_is_used_only_for_its_own_sources(tmp_path, monkeypatch):
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+        rec = json.load(fh)
+    assert rec["bytes_per_launch"] == rec["split_kernel_bytes"] + rec["combine_kernel_bytes"]
+    csrc = _copy_csrc(tmp_path)
+    (tmp_path / "profiles").mkdir()
+    rec["source_sha"] = _sha_at(monkeypatch, tmp_path)
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.ncu_traffic() == rec
+    f = csrc / "combine_note.h"
+    f.write_text("#pragma once\nconstexpr int kChanged = 1;\n")
+    assert bench.ncu_traffic() is None
+
+
+def test_e2e_slot_count_is_an_option(monkeypatch):
+    monkeypatch.setattr("sys.argv", ["bench.py"])
+    assert bench.parse_args().e2e_slots == bench.E2E_SLOTS
+    monkeypatch.setattr("sys.argv", ["bench.py", "--e2e-slots", "2"])
+    assert bench.parse_args().e2e_slots == 2
