@@ -85,7 +85,10 @@ def parse_args():
                     help="rotating input sets (profiling runs use 1 to stay small)")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESCS), default=WORKLOAD,
                     help="the TP2 decode batch is the headline; the others are for the record")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.e2e_slots < 1:
+        ap.error("--e2e-slots must be at least 1")
+    return args
 
 
 def dist_setup(n_gpus):

@@ -11,6 +11,8 @@ import json
 import os
 import shutil
 
+import pytest
+
 import bench
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -59,3 +61,6 @@ def test_e2e_slot_count_is_an_option(monkeypatch):
     assert bench.parse_args().e2e_slots == bench.E2E_SLOTS
     monkeypatch.setattr("sys.argv", ["bench.py", "--e2e-slots", "2"])
     assert bench.parse_args().e2e_slots == 2
+    monkeypatch.setattr("sys.argv", ["bench.py", "--e2e-slots", "0"])
+    with pytest.raises(SystemExit):
+        bench.parse_args()
