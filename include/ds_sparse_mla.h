@@ -261,8 +261,9 @@ int ds_sparse_mla_decode_noalloc(const void* q, const void* kv_pages, int kv_dty
  *  workspace        >= ds_sparse_mla_swa_workspace_size(num_rows, num_heads,
  *                   k, swa_width) bytes, 256-byte aligned.
  *
- * The window entries form their own split(s) after the top-k splits, so the
- * reduction order depends on k and swa_width only, never on the batch.
+ * The concatenated list is cut into 64-entry tiles spread evenly over
+ * max(ceil(k / 512), ceil((k + swa_width) / 768)) splits, so the reduction
+ * order depends on k and swa_width only, never on the batch.
  */
 int ds_sparse_mla_decode_swa(const void* q, const void* kv_pages, int kv_dtype, int64_t num_pages,
                              const int32_t* block_table, int64_t bt_stride, const int32_t* idx,

@@ -180,3 +180,34 @@ def test_kv_cache_write_rejects_bad_arguments(L):
     assert _write(L, slots=A + 4) == DS_ERR_ALIGN and "slots" in _err(L)
     # Zero rows is a valid empty call: nothing is launched.
     assert _write(L, n=0, latent=None, slots=None) == DS_OK
+
+
+def _swa(L, width=128, swa_pages=A, swa_np=8, swa_bt=A, swa_bts=2, swa_idx=A, swa_lens=A,
+         sink=None, wsb=1 << 40, R=4):
+    return L.ds_sparse_mla_decode_swa(A, A, 0, 16, A, 8, A, A, 2048, swa_pages, swa_np, swa_bt,
+                                      swa_bts, swa_idx, swa_lens, width, sink, R, 64, 0.04, A, A,
+                                      A, wsb, None, None)
+
+
+def test_decode_swa_rejects_bad_window_arguments(L):
+    # "Make DSV4 sparse MLA work end-to-end", "What is fixed": the window
+    # index list is padded to a multiple of 64 entries.
+    for width in (32, 100, 576, -64):
+        assert _swa(L, width=width) == DS_ERR_UNSUPPORTED and "swa_width" in _err(L), width
+    assert _swa(L, swa_np=0) == DS_ERR_SHAPE and "swa_num_pages" in _err(L)
+    assert _swa(L, swa_bts=0) == DS_ERR_SHAPE and "swa_bt_stride" in _err(L)
+    for name in ("swa_pages", "swa_bt", "swa_idx", "swa_lens"):
+        assert _swa(L, **{name: None}) == DS_ERR_NULL, name
+    assert _swa(L, swa_pages=A + 8) == DS_ERR_ALIGN and "swa_pages" in _err(L)
+    assert _swa(L, sink=A + 2) == DS_ERR_ALIGN and "attn_sink" in _err(L)
+    need = L.ds_sparse_mla_swa_workspace_size(4, 64, 2048, 128)
+    # Splits: max(ceil(k / 512), ceil((k + W) / 768)); a window adds one only
+    # when the second term wins (k 512 + W 512: 2 splits instead of 1).
+    assert need == L.ds_sparse_mla_workspace_size(4, 64, 2048)
+    assert (L.ds_sparse_mla_swa_workspace_size(4, 64, 512, 512) ==
+            2 * L.ds_sparse_mla_workspace_size(4, 64, 512))
+    assert _swa(L, wsb=need - 1) == DS_ERR_WORKSPACE and str(need) in _err(L)
+    assert L.ds_sparse_mla_swa_workspace_size(4, 64, 2048, 100) == 0
+    # No window: the window arguments may be NULL.
+    assert _swa(L, width=0, swa_pages=None, swa_bt=None, swa_idx=None, swa_lens=None,
+                wsb=1) == DS_ERR_WORKSPACE
