@@ -15,10 +15,17 @@ LSE_ATOL = 1e-2
 
 
 def ensure_built():
+    """The package, with its library built from the current sources (rebuilt
+    when missing or older than any kernel source or public header)."""
+    import glob
+    import os
     import invariant_sparse_mla_gb300 as ds
     from invariant_sparse_mla_gb300 import build as b
-    import os
-    if not os.path.exists(b.lib_path()):
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sources = (glob.glob(os.path.join(root, "invariant_sparse_mla_gb300", "csrc", "*")) +
+               glob.glob(os.path.join(root, "include", "*.h")))
+    lib = b.lib_path()
+    if not os.path.exists(lib) or os.path.getmtime(lib) < max(map(os.path.getmtime, sources)):
         b.build()
     return ds
 
