@@ -211,3 +211,22 @@ def test_decode_swa_rejects_bad_window_arguments(L):
     # No window: the window arguments may be NULL.
     assert _swa(L, width=0, swa_pages=None, swa_bt=None, swa_idx=None, swa_lens=None,
                 wsb=1) == DS_ERR_WORKSPACE
+
+
+def test_split_geometry_fits_the_kernels(L):
+    # The split count is a function of k and the window width alone:
+    # S = max(ceil(k / 512), ceil((k + W) / 768)). The split kernel holds at
+    # most 12 tiles of 64 entries per split and the combine merges at most 4
+    # splits, so every supported (k, W) must satisfy both. S is read back from
+    # the workspace size (S x R x H x (512 + 2) floats, the m and l arrays
+    # padded to 256 bytes).
+    R, H = 1, 64
+    for k in range(64, 2049, 64):
+        for W in [0] + list(range(64, 513, 64)):
+            ws = L.ds_sparse_mla_swa_workspace_size(R, H, k, W)
+            S = -(-k // 512)
+            S = max(S, -(-(k + W) // 768))
+            ml = -(-(S * R * H * 4) // 256) * 256
+            assert ws == S * R * H * 512 * 4 + 2 * ml, (k, W)
+            T = (k + W) // 64
+            assert S <= 4 and -(-T // S) <= 12, (k, W, S, T)
