@@ -67,7 +67,7 @@ WORKLOAD_DESCS = {
 }
 METRIC = "sparse-MLA decode tokens/s and top-k rows/s on 1 GB300; % of roofline"
 N_SETS = 4
-E2E_SLOTS = 4   # steps in flight end to end: 2 -> 500 K, 3 -> 708 K, 4 -> 813 K tokens/s measured
+E2E_SLOTS = 4   # steps in flight end to end: 2 -> 500 K, 3 -> 708 K, 4 -> 816 K, 6 -> 786 K tokens/s measured
 HBM_CONTRACT_GBS = 8000.0
 
 
