@@ -12,16 +12,20 @@ heads, contexts uniform in [4096, 32768], top-k 2048, bf16 latent KV in
 
 Prints one JSON line on rank 0. `value` is decode tokens/s of the whole job
 (one token = one request row per step, all heads), measured with CUDA events
-around K steps replayed from a CUDA graph, inputs resident in HBM. Four
-independent input sets rotate so the gathered KV (4 x 75.5 MB) exceeds the
-129 MB L2 between reuses. `e2e` repeats the step through the public API with
-pinned host buffers: the step's inputs are copied host->device, and out, lse
-and idx are read back, inside the timed region, with four steps in flight on
-four streams (copies run at about 200 GB/s, so one step's 9 MB of transfers
-take about as long as its kernels). Independent steps' kernels then overlap
-too, so `e2e` can exceed the single-stream `value`. Under torchrun every rank
-runs its own batch (rows are independent: weak scaling, no collective on the
-data path).
+around exactly K steps (after exactly W warm-up steps) replayed from CUDA
+graphs, inputs resident in HBM. Four independent input sets rotate so the
+gathered KV (4 x 75.5 MB) exceeds the 129 MB L2 between reuses. The same step
+keeps running for a second after the timed region so that the nvidia-smi
+clock record holds samples under this load. `e2e` repeats the step through
+the public API with pinned host buffers: the step's inputs are copied
+host->device, and out, lse and idx are read back, inside the timed region,
+with four steps in flight on four streams (copies run at about 200 GB/s, so
+one step's 9 MB of transfers take about as long as its kernels); it runs at
+least 200 steps and 0.5 s. Independent steps' kernels then overlap too, so
+`e2e` can exceed the single-stream `value`. The default run also measures
+the TP1 FP8 decode batch and the chunked-prefill chunk (`other_configs`, each
+with its own roofline blocks). Under torchrun every rank runs its own batch
+(rows are independent: weak scaling, no collective on the data path).
 
 `--impl reference` times the CPU oracle (test infrastructure, the
 reference arm of this comparison) on bounded samples of the same workload.
@@ -68,6 +72,12 @@ WORKLOAD_DESCS = {
 METRIC = "sparse-MLA decode tokens/s and top-k rows/s on 1 GB300; % of roofline"
 N_SETS = 4
 E2E_SLOTS = 4   # steps in flight end to end: 2 -> 500 K, 3 -> 708 K, 4 -> 816 K, 6 -> 786 K tokens/s measured
+E2E_MIN_STEPS = 200
+E2E_MIN_SECS = 0.5
+CLOCK_WINDOW_S = 1.0
+CPU_BASELINE_S = 10.0
+REFERENCE_CAP_S = 120.0
+EXTRA_STEPS = {"tp1_fp8_decode": 100, "chunked_prefill": 20}
 HBM_CONTRACT_GBS = 8000.0
 
 
@@ -79,6 +89,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the TP1 FP8 decode and chunked-prefill lines of the default run")
     ap.add_argument("--e2e-slots", type=int, default=E2E_SLOTS,
                     help="steps in flight in the end-to-end loop (each its own stream and buffers)")
     ap.add_argument("--sets", type=int, default=N_SETS,
@@ -88,6 +100,8 @@ def parse_args():
     args = ap.parse_args()
     if args.e2e_slots < 1:
         ap.error("--e2e-slots must be at least 1")
+    if args.steps < 1 or args.warmup < 0 or args.sets < 1:
+        ap.error("--steps must be at least 1, --warmup at least 0, --sets at least 1")
     return args
 
 
@@ -150,18 +164,20 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic():
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel sources; else None."""
+def ncu_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` ("attention" or "topk") on
+    `workload` from the committed ncu summary, if it was taken on the current
+    kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        if t.get("source_sha") == kernel_source_sha():
-            return t
+        if t.get("source_sha") != kernel_source_sha():
+            return None
+        rec = t["records"].get(f"{workload}:{kernel}")
+        return int(rec["bytes_per_launch"]) if rec else None
     except Exception:
-        pass
-    return None
+        return None
 
 
 class ClockSampler:
@@ -260,58 +276,60 @@ def algorithmic_bytes(case, idx):
     return topk, attn, flops
 
 
-def run_ours(args, rank, world, local):
+def job_value(world, rows_per_rank, steps, secs):
+    """Whole-job throughput: the rows all ranks processed in `steps` steps,
+    over the slowest rank's time (`secs`, already the max over ranks)."""
+    return world * rows_per_rank * steps / secs
+
+
+def build_sets(wl, n_sets, rank, device):
+    """`n_sets` independent input sets of workload `wl` (shifted seeds per
+    set and rank; set 0 of rank 0 is the workload's own seed), each with its
+    idx, out, lse and workspace buffers."""
     import torch
     import invariant_sparse_mla_gb300 as ds
-    from synthetic import workload_case
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    sets = []
-    n_sets = args.sets
     from synthetic import WORKLOADS, decode_case, prefill_case, mtp_case, window_case, _uniform_ints
-    wl = args.workload
     w = WORKLOADS[wl]
+    sets = []
     for s in range(n_sets):
-        # Independent batches per set and rank: the same recipe, shifted seeds.
         seed = w["seed"] + 1000 * rank + 17 * s
+        own = s == 0 and rank == 0
         if w["kind"] in ("decode", "decode_swa"):
-            ctx = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if s == 0 and rank == 0
-                                else seed)
-            c = decode_case(wl, ctx, w["H"], w["k"], w["kv"], seed if s or rank else w["seed"],
-                            w["scores"], stride=w["stride"], device="cuda")
+            ctx = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if own else seed)
+            c = decode_case(wl, ctx, w["H"], w["k"], w["kv"], w["seed"] if own else seed,
+                            w["scores"], stride=w["stride"], device=device)
             if w["kind"] == "decode_swa":
                 # The window cache holds each request's last swa_width tokens.
                 c.win = window_case([min(n, w["swa_width"]) for n in ctx], w["swa_width"], w["kv"],
-                                    seed + 7, device="cuda")
-                c.sink = torch.randn(w["H"], generator=torch.Generator().manual_seed(seed)).cuda()
+                                    seed + 7, device=device)
+                c.sink = torch.randn(w["H"], generator=torch.Generator().manual_seed(seed)).to(device)
         elif w["kind"] == "mtp":
-            lens = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if s == 0 and rank == 0
-                                 else seed)
-            c = mtp_case(wl, lens, w["next_n"], w["H"], w["k"], w["kv"],
-                         seed if s or rank else w["seed"], w["scores"], stride=w["stride"],
-                         device="cuda")
+            lens = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if own else seed)
+            c = mtp_case(wl, lens, w["next_n"], w["H"], w["k"], w["kv"], w["seed"] if own else seed,
+                         w["scores"], stride=w["stride"], device=device)
         else:
             c = prefill_case(wl, w["ctx"], w["first_pos"], w["T"], w["H"], w["k"], w["kv"],
-                             seed if s or rank else w["seed"], device="cuda")
+                             w["seed"] if own else seed, device=device)
         R, H, k = c.q.shape[0], c.H, c.k
-        c.idx = torch.empty((R, k), dtype=torch.int32, device=dev)
-        c.out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
-        c.lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+        c.idx = torch.empty((R, k), dtype=torch.int32, device=device)
+        c.out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=device)
+        c.lse = torch.empty((R, H), dtype=torch.float32, device=device)
         c.ws = torch.empty(ds.swa_workspace_size(R, H, k, w.get("swa_width", 0)),
-                           dtype=torch.uint8, device=dev)
+                           dtype=torch.uint8, device=device)
         sets.append(c)
-    R, H, k = sets[0].q.shape[0], sets[0].H, sets[0].k
-    stream = torch.cuda.Stream(device=dev)
+    return sets
 
+
+def make_calls(ds, kind, stream):
+    """The public calls of one step: top-k, then the attention call."""
     def topk(c):
         ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k, idx_out=c.idx, stream=stream)
 
     def decode(c):
-        if w["kind"] == "decode":
+        if kind == "decode":
             ds.sparse_mla_decode(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.idx, c.lens,
                                  c.scale, out=c.out, lse=c.lse, workspace=c.ws, stream=stream)
-        elif w["kind"] == "decode_swa":
+        elif kind == "decode_swa":
             ds.sparse_mla_decode_swa(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.idx, c.lens,
                                      c.scale, swa_pages=c.win[0], swa_block_table=c.win[1],
                                      swa_idx=c.win[2], swa_lens=c.win[3], attn_sink=c.sink,
@@ -325,40 +343,153 @@ def run_ours(args, rank, world, local):
         topk(c)
         decode(c)
 
-    # Warm up eagerly (also resolves lazy module loading), then capture graphs.
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            for c in sets:
-                step(c)
-    stream.synchronize()
+    return topk, decode, step
 
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for c in sets:
-                fn(c)
-        return g
 
-    g_step, g_topk, g_dec = capture(step), capture(topk), capture(decode)
-    reps = max(1, math.ceil(args.steps / n_sets))
-    steps = reps * n_sets
-    wreps = max(1, math.ceil(max(args.warmup, 3) / n_sets))
+class Replayer:
+    """Runs any number of steps exactly, cycling through the input sets in
+    order: whole passes over the sets replay one CUDA graph of all of them
+    (consecutive steps keep their programmatic-launch overlap), the rest
+    replay one graph per set."""
 
-    def timed(graph, n):
+    def __init__(self, stream, fn, sets):
+        import torch
+        self.stream = stream
+
+        def capture(cases):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in cases:
+                    fn(c)
+            return g
+
+        self.cycle = capture(sets)
+        self.single = [capture([c]) for c in sets]
+        self.n = len(sets)
+        self.pos = 0
+
+    def run(self, steps):
+        import torch
+        with torch.cuda.stream(self.stream):   # replay() launches on the current stream
+            i = 0
+            while i < steps:
+                if self.pos == 0 and steps - i >= self.n:
+                    self.cycle.replay()
+                    i += self.n
+                else:
+                    self.single[self.pos].replay()
+                    self.pos = (self.pos + 1) % self.n
+                    i += 1
+
+    def timed(self, steps):
+        """Seconds for `steps` steps, by CUDA events on the launching stream."""
+        import torch
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):   # replay() launches on the current stream
-            e0.record(stream)
-            for _ in range(n):
-                graph.replay()
-            e1.record(stream)
+        e0.record(self.stream)
+        self.run(steps)
+        e1.record(self.stream)
         e1.synchronize()
         return e0.elapsed_time(e1) / 1e3
 
+
+def per_call_seconds(rep, calls):
+    """Mean seconds per call over `calls` calls (at least one whole pass)."""
+    n = max(rep.n, calls // rep.n * rep.n)
+    rep.run(rep.n)   # warm
+    return rep.timed(n) / n
+
+
+def roofline_block(kind, bytes_or_flops, secs, hbm, tflops, peak_kind, kernel, traffic=None):
+    if kind == "hbm":
+        gbs = bytes_or_flops / secs / 1e9
+        return {"bound": "hbm", "kernel": kernel, "achieved": round(gbs, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": f"{peak_kind} HBM copy",
+                "traffic": traffic, "algorithmic_bytes": round(bytes_or_flops)}
+    tf = bytes_or_flops / secs / 1e12
+    return {"bound": "tensor", "kernel": kernel, "achieved": round(tf, 1), "peak": tflops,
+            "unit": "TFLOP/s", "frac": round(tf / tflops, 4),
+            "peak_kind": f"{peak_kind} bf16 dense (burst)", "traffic": traffic,
+            "algorithmic_flops": round(bytes_or_flops)}
+
+
+def contract_fraction(attn_bytes, attn_flops, secs, tflops):
+    """Fraction of the contract roofline max(bytes / 8 TB/s, flops / bf16 peak)."""
+    roof_s = max(attn_bytes / (HBM_CONTRACT_GBS * 1e9), attn_flops / (tflops * 1e12))
+    return round(roof_s / secs, 4)
+
+
+def measure_extra(ds, wl, dev, stream, steps, warmup):
+    """Another workload on this GPU, for the record: one input set (its
+    per-step traffic alone exceeds L2), `warmup` then `steps` steps replayed
+    from CUDA graphs, and the two calls timed alone. Returns a dict for the
+    JSON line."""
+    import torch
+    from synthetic import WORKLOADS
+    w = WORKLOADS[wl]
+    sets = build_sets(wl, 1, 0, dev)
+    topk, decode, step = make_calls(ds, w["kind"], stream)
     with torch.cuda.stream(stream):
-        for _ in range(wreps):
-            g_step.replay()
+        for _ in range(2):
+            step(sets[0])
+    stream.synchronize()
+    rs, rt, rd = (Replayer(stream, f, sets) for f in (step, topk, decode))
+    rs.run(warmup)
+    secs = rs.timed(steps)
+    topk_s = per_call_seconds(rt, steps)
+    dec_s = per_call_seconds(rd, steps)
+    c = sets[0]
+    tb, ab, fl = algorithmic_bytes(c, c.idx)
+    hbm, tflops, peak_kind = load_peaks()
+    R = c.q.shape[0]
+    res = {"workload": WORKLOAD_DESCS[wl], "rows": R, "heads": c.H, "topk": c.k,
+           "kv_dtype": c.kv_dtype, "steps": steps, "warmup": warmup,
+           "step_us": round(secs / steps * 1e6, 3), "tokens_per_s": round(R * steps / secs, 1),
+           "topk_us": round(topk_s * 1e6, 3), "attention_us": round(dec_s * 1e6, 3),
+           "roofline_topk": roofline_block("hbm", tb, topk_s, hbm, tflops, peak_kind,
+                                           "ds_topk_per_row", ncu_traffic(wl, "topk")),
+           "roofline": roofline_block("tensor", fl, dec_s, hbm, tflops, peak_kind,
+                                      "sparse_mla attention (split + combine)",
+                                      ncu_traffic(wl, "attention")),
+           "attention_algorithmic_bytes": round(ab),
+           "frac_of_contract_roofline": contract_fraction(ab, fl, dec_s, tflops),
+           "l2": "1 input set; its per-step traffic exceeds the 129 MB L2"}
+    del rs, rt, rd, sets, c
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+EXTRA_WORKLOADS = ("tp1_fp8_decode", "chunked_prefill")
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import invariant_sparse_mla_gb300 as ds
+    from synthetic import WORKLOADS
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = args.workload
+    w = WORKLOADS[wl]
+    n_sets = args.sets
+    sets = build_sets(wl, n_sets, rank, dev)
+    R, H, k = sets[0].q.shape[0], sets[0].H, sets[0].k
+    stream = torch.cuda.Stream(device=dev)
+    topk, decode, step = make_calls(ds, w["kind"], stream)
+
+    # Eager calls first (they also resolve lazy module loading), then graphs.
+    with torch.cuda.stream(stream):
+        for c in sets:
+            step(c)
+    stream.synchronize()
+    rep_step = Replayer(stream, step, sets)
+    rep_topk = Replayer(stream, topk, sets)
+    rep_dec = Replayer(stream, decode, sets)
+
+    steps, warmup = args.steps, args.warmup
+    rep_step.run(warmup)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(gpu_id_for_smi(local))
@@ -366,53 +497,56 @@ def run_ours(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    secs = timed(g_step, reps)
+    secs = rep_step.timed(steps)
+    # The timed region of a short run is far below nvidia-smi's sampling
+    # period: the same step keeps running for another second so the clock
+    # record holds samples taken under this load.
+    t_load = time.time()
+    while time.time() - t_load < CLOCK_WINDOW_S:
+        rep_step.run(max(n_sets, 256 // n_sets * n_sets))
+        stream.synchronize()
     t1 = time.time()
     barrier(world)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
+    clocks["window"] = (f"the timed region plus {t1 - t_load:.2f} s of the same step "
+                        "replayed right after it")
     secs = max_over_ranks(secs, world)
 
-    # Per-kernel averages (graphs of one call per input set).
-    n_k = max(8, min(500, reps))
-    topk_s = timed(g_topk, n_k) / (n_k * n_sets)
-    dec_s = timed(g_dec, n_k) / (n_k * n_sets)
+    # Per-call averages (graphs of one call per input set).
+    n_k = max(8 * n_sets, min(500, steps))
+    topk_s = per_call_seconds(rep_topk, n_k)
+    dec_s = per_call_seconds(rep_dec, n_k)
 
     # Work per step (mean over the input sets).
     tb, ab, fl = zip(*[algorithmic_bytes(c, c.idx) for c in sets])
     topk_bytes, attn_bytes, attn_flops = (sum(tb) / n_sets, sum(ab) / n_sets, sum(fl) / n_sets)
 
     # End to end through the public API with pinned host buffers.
-    e2e = None if (args.no_e2e or w["kind"] != "decode") else run_e2e(ds, sets, stream, dev,
-                                           steps_e2e=max(20, min(400, args.steps // 50)),
-                                           n_slots=args.e2e_slots,
-                                           world=world)
+    e2e = None if (args.no_e2e or w["kind"] != "decode") else run_e2e(
+        ds, sets, stream, dev, min_steps=E2E_MIN_STEPS, min_secs=E2E_MIN_SECS,
+        n_slots=args.e2e_slots, world=world)
 
     hbm, tflops, peak_kind = load_peaks()
-    value = world * R * steps / secs
+    value = job_value(world, R, steps, secs)
     ms_per_step = secs / steps * 1e3
     launches = steps * 3  # top-k + split + combine
-    attn_gbs = attn_bytes / dec_s / 1e9
-    topk_gbs = topk_bytes / topk_s / 1e9
-    roof_s = max(attn_bytes / (HBM_CONTRACT_GBS * 1e9), attn_flops / (tflops * 1e12))
     tensor_bound = attn_flops / (tflops * 1e12) > attn_bytes / (hbm * 1e9)
-    attn_tflops = attn_flops / dec_s / 1e12
+    frac_contract = contract_fraction(attn_bytes, attn_flops, dec_s, tflops)
     if tensor_bound:
-        roof = {"bound": "tensor", "kernel": "sparse_mla attention (split + combine)",
-                "achieved": round(attn_tflops, 1), "peak": tflops, "unit": "TFLOP/s",
-                "frac": round(attn_tflops / tflops, 4), "peak_kind": f"{peak_kind} bf16 dense",
-                "traffic": None, "algorithmic_flops": round(attn_flops),
-                "frac_of_contract_roofline": round(roof_s / dec_s, 4)}
+        roof = roofline_block("tensor", attn_flops, dec_s, hbm, tflops, peak_kind,
+                              "sparse_mla attention (split + combine)", ncu_traffic(wl, "attention"))
     else:
-        roof = None
-    traffic = ncu_traffic()
+        roof = roofline_block("hbm", attn_bytes, dec_s, hbm, tflops, peak_kind,
+                              "sparse_mla_decode (split + combine)", ncu_traffic(wl, "attention"))
+    roof["frac_of_contract_roofline"] = frac_contract
     line = {
         "metric": METRIC if wl == WORKLOAD else METRIC + f" [{wl}]",
         "value": round(value, 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": steps,
-        "warmup": wreps * n_sets,
+        "warmup": warmup,
         "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True,
         "scaling": "weak",
@@ -427,30 +561,26 @@ def run_ours(args, rank, world, local):
         "decode_tokens_per_s": round(world * R / dec_s, 1),
         "topk_us": round(topk_s * 1e6, 3),
         "decode_us": round(dec_s * 1e6, 3),
-        "roofline": {"bound": "hbm", "kernel": "sparse_mla_decode (split + combine)",
-                     "achieved": round(attn_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(attn_gbs / hbm, 4), "peak_kind": f"{peak_kind} HBM copy",
-                     "traffic": (round(traffic["bytes_per_launch"]) if traffic else None),
-                     "algorithmic_bytes": round(attn_bytes),
-                     "frac_of_contract_roofline": round(roof_s / dec_s, 4)},
-        "roofline_topk": {"bound": "hbm", "achieved": round(topk_gbs, 1), "peak": hbm,
-                          "unit": "GB/s", "frac": round(topk_gbs / hbm, 4),
-                          "algorithmic_bytes": round(topk_bytes)},
+        "roofline": roof,
+        "roofline_topk": roofline_block("hbm", topk_bytes, topk_s, hbm, tflops, peak_kind,
+                                        "ds_topk_per_row", ncu_traffic(wl, "topk")),
         "e2e": e2e,
-        "attention_tflops": round(attn_tflops, 1),
+        "attention_tflops": round(attn_flops / dec_s / 1e12, 1),
         "gpu_launches": launches,
         "clocks": clocks,
     }
-    if roof is not None:
-        line["roofline"] = roof
-    if wl != WORKLOAD or traffic is None:
-        line["roofline"]["traffic"] = None
     if rank == 0 and not args.no_cpu_baseline and world == 1 and wl == WORKLOAD:
-        line["cpu_baseline"] = cpu_baseline(sets[0], budget_s=10.0)
+        line["cpu_baseline"] = cpu_baseline(sets[0], budget_s=CPU_BASELINE_S)
+    if wl == WORKLOAD and not args.no_extra:
+        del rep_step, rep_topk, rep_dec, sets
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["other_configs"] = {x: measure_extra(ds, x, dev, stream, EXTRA_STEPS[x], 3)
+                                 for x in EXTRA_WORKLOADS}
     return line
 
 
-def run_e2e(ds, sets, stream, dev, steps_e2e, world, n_slots=E2E_SLOTS):
+def run_e2e(ds, sets, stream, dev, min_steps, min_secs, world, n_slots=E2E_SLOTS):
     """Host -> device inputs, the two calls, device -> host results, every step.
 
     A serving loop: each step's inputs (scores, row bounds, q, block table,
@@ -459,7 +589,8 @@ def run_e2e(ds, sets, stream, dev, steps_e2e, world, n_slots=E2E_SLOTS):
     `n_slots` steps are in flight (slots used in turn, each on its own stream),
     so one step's transfers overlap another's kernels. Before a slot is reused
     the host waits for that slot's previous download, so every step's result
-    is on the host within the timed region.
+    is on the host within the timed region. The loop runs at least
+    `min_steps` steps and at least `min_secs` seconds (checked between steps).
     """
     import torch
     in_names = ("scores", "row_starts", "row_ends", "q", "block_table", "lens")
@@ -536,7 +667,7 @@ def run_e2e(ds, sets, stream, dev, steps_e2e, world, n_slots=E2E_SLOTS):
         si = i % n_slots
         sl = slots[si]
         if sl["used"]:
-            sl["out_done"].synchronize()   # the host has step i - 2's result
+            sl["out_done"].synchronize()   # the host has step i - n_slots's result
         with torch.cuda.stream(streams[si]):
             sl["graphs"][i % len(sets)].replay()
             sl["out_done"].record(streams[si])
@@ -553,13 +684,16 @@ def run_e2e(ds, sets, stream, dev, steps_e2e, world, n_slots=E2E_SLOTS):
     barrier(world)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    for i in range(steps_e2e):
-        one(i)
+    n = 0
+    while n < min_steps or time.perf_counter() - t0 < min_secs:
+        one(n)
+        n += 1
     drain()
     secs = max_over_ranks(time.perf_counter() - t0, world)
     R = sets[0].q.shape[0]
-    return {"value": round(world * R * steps_e2e / secs, 1), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps_e2e,
+    return {"value": round(job_value(world, R, n, secs), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "seconds": round(secs, 3),
             "timing": "host wall clock from the first upload to the last result on the host",
             "pipelining": f"{n_slots} steps in flight; each step is one CUDA graph of the public "
                           "calls (upload, top-k, decode, download), each slot on its own stream",
@@ -585,68 +719,75 @@ def oracle_sample_inputs(case, rows):
     return scores, starts, ends, q, kv, bt2, lens
 
 
-def oracle_step(inputs, k, scale, heads=None):
+def oracle_step(inputs, k, scale):
     import oracle
     scores, starts, ends, q, kv, bt, lens = inputs
     idx = oracle.topk_per_row(scores, starts, ends, k)
-    if heads is not None:
-        q = q[:, heads]
     return oracle.sparse_mla_decode(q, kv, "bf16", bt, idx, lens, scale)
+
+
+class OracleBatch:
+    """The oracle over one decode batch, row by row (top-k, then float64
+    attention over all heads): the CPU side of both the `cpu_baseline` leg
+    and the reference arm, so the two time the same work the same way."""
+
+    def __init__(self, case):
+        self.case = case
+        self.R = case.q.shape[0]
+        self.inputs = [oracle_sample_inputs(case, [r]) for r in range(self.R)]
+
+    def run(self):
+        """One step: every row of the batch once. Returns the seconds taken."""
+        t0 = time.perf_counter()
+        for inp in self.inputs:
+            oracle_step(inp, self.case.k, self.case.scale)
+        return time.perf_counter() - t0
 
 
 def cpu_baseline(case, budget_s):
     """The oracle on the host cores over a bounded sample of the workload:
-    decode rows of one input set, cycled until `budget_s` of oracle time."""
+    whole passes over one input set's decode batch, one untimed pass first,
+    then timed passes until `budget_s` seconds of oracle time."""
     cores = len(os.sched_getaffinity(0))
-    R = case.q.shape[0]
-    cache = {}
-    done, t_used = 0, 0.0
-    while t_used < budget_s and done < 100000:
-        r = done % R
-        if r not in cache:
-            cache[r] = oracle_sample_inputs(case, [r])
-        t0 = time.perf_counter()
-        oracle_step(cache[r], case.k, case.scale)
-        t_used += time.perf_counter() - t0
-        done += 1
-    return {"value": round(done / t_used, 3), "unit": "tokens/s", "cores": cores,
+    ob = OracleBatch(case)
+    ob.run()
+    t_used, passes = 0.0, 0
+    while t_used < budget_s:
+        t_used += ob.run()
+        passes += 1
+    return {"value": round(passes * ob.R / t_used, 3), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{done} decode-row computations (the {R} rows of input set 0, cycled; "
-                      f"top-k + float64 attention over all heads), {t_used:.1f} s of oracle "
-                      f"time; numpy BLAS may use all {cores} host cores"}
+            "sample": f"{passes} passes over the {ob.R}-row batch of input set 0 (top-k + float64 "
+                      f"attention over all heads, row by row) after one untimed pass, "
+                      f"{t_used:.1f} s of oracle time; numpy BLAS may use all {cores} host cores"}
 
 
 def run_reference(args, rank, world):
-    """Reference arm: the CPU oracle, one decode row of the batch per step."""
+    """Reference arm: the CPU oracle; one step = one pass over the decode
+    batch (every row: top-k + float64 attention over all heads)."""
     if rank != 0:
         return None
     from synthetic import workload_case
     case = workload_case(WORKLOAD, device="cpu")
-    R, H = case.q.shape[0], case.H
+    H = case.H
     cores = len(os.sched_getaffinity(0))
-    cache = {}
+    ob = OracleBatch(case)
+    for _ in range(args.warmup):
+        ob.run()
     t_used, n = 0.0, 0
-    cap_s = 120.0   # bounds the run when --steps is large
-    for i in range(args.warmup + args.steps):
-        r = i % R
-        if r not in cache:
-            cache[r] = oracle_sample_inputs(case, [r])
-        t0 = time.perf_counter()
-        oracle_step(cache[r], case.k, case.scale)
-        dt = time.perf_counter() - t0
-        if i >= args.warmup:
-            t_used += dt
-            n += 1
-            if t_used > cap_s:
-                break
-    value = n / t_used
-    sample = (f"{n} timed steps, each one decode row of the {R}-row batch (rows cycled): "
-              f"top-k + float64 attention over all {H} heads, {t_used:.1f} s")
+    for _ in range(args.steps):
+        t_used += ob.run()
+        n += 1
+        if t_used > REFERENCE_CAP_S:   # bounds the run when --steps is large
+            break
+    value = n * ob.R / t_used
+    sample = (f"{n} timed steps after {args.warmup} untimed, each one pass over the {ob.R}-row "
+              f"decode batch: top-k + float64 attention over all {H} heads, {t_used:.1f} s")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
             "n_gpus": world, "steps": n, "steps_requested": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t_used / max(n, 1) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": WORKLOAD_DESCS[WORKLOAD], "global_batch": R,
+            "config": {"workload": WORKLOAD_DESCS[WORKLOAD], "global_batch": ob.R,
                        "parallelism": "CPU oracle, rank 0"},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
                              "kind": "oracle", "sample": sample},

@@ -219,7 +219,9 @@ int ds_sparse_mla_prefill(const void* q, const void* kv_pages, int kv_dtype, int
  * itself performs no cudaMalloc/cudaFree or other allocation.
  *
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * that device current); make that first call before any stream capture. A
+ * lookup that fails returns DS_ERR_CUDA and is not remembered: the next call
+ * tries again.
  * Every call shares the one array, and each call overwrites what the
  * previous one left there: calls that can overlap on the GPU (on different
  * streams without ordering between them) race on it and must not be issued.

@@ -778,8 +778,14 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   if (tid < 128) cp_async_wait_all();   // Q copies, on every path
   if (failed && p.err != nullptr) atomicOr(p.err, kErrTimeout);
   tc_fence_before();
-  __syncthreads();
+  const bool cta_failed = __syncthreads_or(failed);
   tc_fence_after();
+  // A split that gave up leaves a NaN m and l, so its row's output is NaN
+  // (never a plausible value built from a previous call's partials).
+  if (cta_failed && tid < HG) {
+    p.part_m[part_base + tid] = __int_as_float(0x7fc00000);
+    p.part_l[part_base + tid] = __int_as_float(0x7fc00000);
+  }
   if (warp == RL::kQkA) tmem_dealloc(tmem, LY::kTmemCols);
 }
 
@@ -823,9 +829,18 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   }
   const float sl = sink != nullptr ? sink[rh % H] * 1.4426950408889634f : -INFINITY;
   float M = sl;
+  bool gave_up = false;   // a split that timed out left NaN partials
 #pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ms[s]);
+  for (int s = 0; s < kMaxSplits; ++s) {
+    M = fmaxf(M, ms[s]);
+    gave_up |= ms[s] != ms[s];
+  }
   __nv_bfloat16* o = out + rh * kDv + 4 * t;
+  if (gave_up) {
+    *reinterpret_cast<uint2*>(o) = make_uint2(0x7fc07fc0u, 0x7fc07fc0u);
+    if (t == 0) lse[rh] = __int_as_float(0x7fc00000);
+    return;
+  }
   if (M == -INFINITY) {
     *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
     if (t == 0) lse[rh] = -INFINITY;
@@ -855,14 +870,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 template <int HG, bool FP8>
 cudaError_t launch_split(const KParams& kp, int64_t blocks, cudaStream_t stream) {
   using LY = Layout<HG>;
-  static std::atomic<bool> attr_set{false};
+  static PerDeviceOnce attr_once;
   auto kern = sparse_mla_split_kernel<HG, FP8>;
-  if (!attr_set.load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         LY::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set.store(true, std::memory_order_release);
-  }
+  int dev = 0;
+  cudaError_t e = stream_device(stream, &dev);
+  if (e == cudaSuccess) e = set_max_dynamic_smem(attr_once, dev, kern, LY::kSmemBytes);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3((unsigned)blocks), dim3(Roles<FP8>::kThreads), LY::kSmemBytes, stream,
                     1u, kp);
 }

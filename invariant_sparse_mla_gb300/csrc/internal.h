@@ -4,6 +4,7 @@
 #include <stdint.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <utility>
 
 namespace dsmla {
@@ -122,5 +123,38 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Records a printf-style message for ds_last_error() on this host thread and
 // returns `status`.
 int report_error(int status, const char* fmt, ...);
+
+// The device a launch on `stream` runs on: the stream's own device, or the
+// current device for the legacy default stream.
+inline cudaError_t stream_device(cudaStream_t stream, int* dev) {
+  if (stream == nullptr) return cudaGetDevice(dev);
+  return cudaStreamGetDevice(stream, dev);
+}
+
+// A kernel attribute (the dynamic shared memory limit) is a per-device
+// setting: it is set once for each device the library launches on, the flag
+// of device d recording that it was. Devices beyond the table are set on
+// every launch.
+struct PerDeviceOnce {
+  static constexpr int kMaxDevices = 64;
+  std::atomic<bool> done[kMaxDevices] = {};
+};
+
+template <typename Kernel>
+cudaError_t set_max_dynamic_smem(PerDeviceOnce& once, int dev, Kernel kernel, int bytes) {
+  const bool tracked = dev >= 0 && dev < PerDeviceOnce::kMaxDevices;
+  if (tracked && once.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  int prev = 0;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return e;
+  if (prev != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (prev != dev) {
+    const cudaError_t e2 = cudaSetDevice(prev);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (e == cudaSuccess && tracked) once.done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 }  // namespace dsmla

@@ -15,7 +15,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "ds_sparse_mla.h"
 #include "internal.h"
@@ -30,12 +30,12 @@ constexpr size_t kScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 // Host code cannot use `g_decode_scratch` as a device address (on the host
-// it names a stand-in object). Its device address is looked up once per
-// device, with that device current, and cached here.
+// it names a stand-in object). Its device address is looked up with the
+// device current and cached here once the lookup has succeeded; a failed
+// lookup (for example one attempted during a stream capture) is not cached
+// and is retried by the next call.
 constexpr int kMaxDevices = 128;
-void* g_scratch_addr[kMaxDevices];
-cudaError_t g_scratch_status[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 }  // namespace
 
@@ -63,13 +63,19 @@ extern "C" int ds_sparse_mla_decode_noalloc(const void* q, const void* kv_pages,
   if (dev < 0 || dev >= kMaxDevices)
     return dsmla::report_error(DS_ERR_UNSUPPORTED, "%s: device %d is beyond the %d supported", fn,
                                dev, kMaxDevices);
-  std::call_once(g_scratch_once[dev], [dev] {
-    g_scratch_status[dev] = cudaGetSymbolAddress(&g_scratch_addr[dev], g_decode_scratch);
-  });
-  if (g_scratch_status[dev] != cudaSuccess)
-    return dsmla::report_error(DS_ERR_CUDA, "%s: cudaGetSymbolAddress of the scratch failed: %s",
-                               fn, cudaGetErrorString(g_scratch_status[dev]));
+  void* scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (scratch == nullptr) {
+    // Two threads may both get here on the first calls; both find the same
+    // address.
+    e = cudaGetSymbolAddress(&scratch, g_decode_scratch);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();   // not sticky: clear it so the next call can retry
+      return dsmla::report_error(DS_ERR_CUDA, "%s: cudaGetSymbolAddress of the scratch failed: %s",
+                                 fn, cudaGetErrorString(e));
+    }
+    g_scratch_addr[dev].store(scratch, std::memory_order_release);
+  }
   return ds_sparse_mla_decode(q, kv_pages, kv_dtype, num_pages, block_table, bt_stride, idx, lens,
-                              num_rows, num_heads, k, scale, out, lse, g_scratch_addr[dev],
-                              kScratchBytes, err_flag, stream);
+                              num_rows, num_heads, k, scale, out, lse, scratch, kScratchBytes,
+                              err_flag, stream);
 }

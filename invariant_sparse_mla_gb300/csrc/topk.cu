@@ -8,9 +8,17 @@
 // the -1 padding follow "[Bugfix] Make DSV4 sparse MLA work end-to-end for
 // plain decode, MTP, and DSpark", section "What is fixed".
 //
-// One CTA owns one row; there is no inter-CTA communication and no spin on
-// another CTA. The selected set is unique (the order is total), so the
-// output is bit-exact and batch-independent by construction.
+// Four kernels, chosen by the shape of the call alone:
+//   topk_smem_kernel     one CTA per row, the whole row in shared memory;
+//   topk_stream_kernel   a persistent grid, each CTA streaming whole rows;
+//   topk_cluster_kernel  one thread-block cluster of up to 8 CTAs per row,
+//                        which exchange histograms and counts through
+//                        distributed shared memory between hardware cluster
+//                        barriers;
+//   topk_rows_kernel     one CTA per row, histogram passes over global memory.
+// No kernel spins on a flag written by another CTA. The selected set is
+// unique (the order is total), so every kernel gives the same bit-exact
+// output, and a row's output never depends on the rest of the batch.
 //
 // Key: the float's bits mapped to an unsigned integer whose order is the
 // float order (sign flipped for non-negatives, all bits flipped for
@@ -1158,30 +1166,22 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
   //  - at least 256 rows of up to 64K: the streaming grid;
   //  - otherwise a cluster of up to 8 CTAs per row (rows of up to 128K);
   //  - longer rows: one CTA per row with passes over global memory.
+  int dev = 0;
+  cudaError_t e = stream_device(stream, &dev);
+  if (e != cudaSuccess) return e;
   if (stride <= kRowMaxLen && rows >= kRowMinRows) {
-    static std::atomic<bool> row_attr{false};
-    if (!row_attr.load(std::memory_order_acquire)) {
-      cudaError_t e = cudaFuncSetAttribute(topk_smem_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)sizeof(RowSmem));
-      if (e != cudaSuccess) return e;
-      row_attr.store(true, std::memory_order_release);
-    }
+    static PerDeviceOnce row_attr;
+    e = set_max_dynamic_smem(row_attr, dev, topk_smem_kernel, (int)sizeof(RowSmem));
+    if (e != cudaSuccess) return e;
     return launch_pdl(topk_smem_kernel, dim3((unsigned)rows), dim3(kRowThreads), sizeof(RowSmem),
                       stream, 1u, scores, stride, starts, ends, k, out);
   }
   if (stride <= kStreamMaxLen && rows >= kStreamMinRows) {
-    static std::atomic<bool> stream_attr{false};
-    if (!stream_attr.load(std::memory_order_acquire)) {
-      cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)sizeof(StreamSmem));
-      if (e != cudaSuccess) return e;
-      stream_attr.store(true, std::memory_order_release);
-    }
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static PerDeviceOnce stream_attr;
+    e = set_max_dynamic_smem(stream_attr, dev, topk_stream_kernel, (int)sizeof(StreamSmem));
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)sms * kStreamCtasPerSm;
     const int64_t grid = rows < slots ? rows : slots;
@@ -1198,14 +1198,10 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
                       stride, starts, ends, k, out);
   }
   const size_t smem = sizeof(ClSmem) + (size_t)per * sizeof(uint32_t);
-  static std::atomic<bool> attr_set{false};
-  if (!attr_set.load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(ClSmem) + kClMaxChunk * sizeof(uint32_t)));
-    if (e != cudaSuccess) return e;
-    attr_set.store(true, std::memory_order_release);
-  }
+  static PerDeviceOnce cl_attr;
+  e = set_max_dynamic_smem(cl_attr, dev, topk_cluster_kernel,
+                           (int)(sizeof(ClSmem) + kClMaxChunk * sizeof(uint32_t)));
+  if (e != cudaSuccess) return e;
   return launch_pdl(topk_cluster_kernel, dim3((unsigned)(rows * C)), dim3(kClThreads), smem, stream,
                     (unsigned)C, scores, stride, starts, ends, k, out);
 }

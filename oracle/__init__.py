@@ -27,7 +27,7 @@ special cases, or identities (uniform scores give the mean of V; a single
 valid entry returns its V row exactly).
 """
 
-from .topk import score_key, row_length, topk_per_row, topk_rank_bruteforce  # noqa: F401
+from .topk import row_length, topk_per_row, topk_rank_bruteforce  # noqa: F401
 from .fp8 import (  # noqa: F401
     e4m3_to_float64,
     bf16_bits_to_float64,

@@ -107,13 +107,3 @@ def topk_rank_bruteforce(values, k):
             sel.append(i)
     return sel
 
-
-def score_key(x):
-    """Composite key of one float score as a Python tuple (smaller = first).
-
-    Exposed for tests that want to compare two (score, index) pairs by hand.
-    """
-    x = float(x)
-    if x != x:
-        return (1, 0.0)
-    return (0, -x if x != 0.0 else 0.0)

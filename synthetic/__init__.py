@@ -287,29 +287,35 @@ def workload_case(name, device="cpu", rows=None):
 
 
 def invariance_batch(batch_size, slot, target_seed=0, batch_seed=4, device="cpu",
-                     H=64, k=2048, target_ctx=16384, max_ctx=32768):
+                     H=64, k=2048, target_ctx=16384, max_ctx=32768, kv_dtype="bf16"):
     """Batch-invariance stress: one fixed request at ``slot`` among random neighbours.
 
     The target request (ctx ``target_ctx``, integer scores 0..7, its q rows and
     its latent rows) is drawn from ``target_seed`` alone, so it is identical
     in every batch. Neighbours draw lengths uniform in [1, max_ctx] from
     ``batch_seed``. Every batch has its own pool and page permutation, so the
-    target's rows sit at different physical pages in each batch.
+    target's rows sit at different physical pages in each batch. With
+    ``kv_dtype="fp8"`` the pool holds 656-byte FP8 rows (the target's rows
+    quantised by the same rule as every other row).
     """
     gt = _gen(target_seed, device)
     t_scores = torch.randint(0, 8, (target_ctx,), generator=gt, device=device).to(torch.float32)
     t_q = _normal((H, D_QK), gt, device).to(torch.bfloat16)
-    t_rows = _normal((target_ctx, D_QK), gt, device).to(torch.bfloat16)
+    t_rows = _normal((target_ctx, D_QK), gt, device)
+    if kv_dtype == "bf16":
+        t_rows = t_rows.to(torch.bfloat16)
+    else:
+        t_rows = quantize_fp8_rows(t_rows[:, :512], t_rows[:, 512:].to(torch.bfloat16))
 
     gb = _gen(batch_seed * 1000 + batch_size, device)
     nb_ctx = torch.randint(1, max_ctx + 1, (batch_size,), generator=gb, device=device).tolist()
     ctx = [target_ctx if i == slot else int(nb_ctx[i]) for i in range(batch_size)]
     bt, num_pages = _block_table(ctx, gb, device)
-    pool = _kv_pool(num_pages, "bf16", gb, device)
+    pool = _kv_pool(num_pages, kv_dtype, gb, device)
     # Place the target's rows into its pages of this batch's pool.
     tp = math.ceil(target_ctx / PAGE)
     pages = bt[slot, :tp].long()
-    pool[pages] = t_rows.reshape(tp, PAGE, D_QK)
+    pool[pages] = t_rows.reshape(tp, PAGE, t_rows.shape[-1])
 
     scores = torch.full((batch_size, max_ctx), float("nan"), dtype=torch.float32, device=device)
     for i in range(batch_size):
@@ -321,7 +327,7 @@ def invariance_batch(batch_size, slot, target_seed=0, batch_seed=4, device="cpu"
     q = _normal((batch_size, H, D_QK), gb, device).to(torch.bfloat16)
     q[slot] = t_q
     ends = torch.tensor(ctx, dtype=torch.int32, device=device)
-    return Case(name=f"invariance_b{batch_size}_s{slot}", H=H, k=k, kv_dtype="bf16",
+    return Case(name=f"invariance_b{batch_size}_s{slot}", H=H, k=k, kv_dtype=kv_dtype,
                 scale=1.0 / math.sqrt(D_QK), scores=scores,
                 row_starts=torch.zeros(batch_size, dtype=torch.int32, device=device),
                 row_ends=ends, q=q, kv_pages=pool, block_table=bt,

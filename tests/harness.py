@@ -13,6 +13,18 @@ ATOL = {"bf16": 2e-2, "fp8": 4e-2}
 RTOL = 1e-2
 LSE_ATOL = 1e-2
 
+# A second, scale-aware bound: per (row, head), max |gpu - ref| over the 512
+# output dims <= RMS_TOL * RMS(ref). On the TP2 decode shape an output
+# element is about N(0, 1/750), so ATOL alone is about half of a typical
+# value and would pass a kernel that is 20 % off everywhere; this bound would
+# not. Its size follows from the kernel's arithmetic: out is rounded to bf16
+# (<= 2^-9 relative, and max|out| over 512 dims is about 4 RMS), P is rounded
+# to bf16 before PV (<= 2^-9 relative per entry, averaging out over the
+# entries), and FP8 rows are dequantised to bf16 (another 2^-9 relative on
+# every K and V element). That predicts about 0.01 RMS; the bounds leave a
+# factor of 3 (bf16) and 6 (FP8) above it.
+RMS_TOL = {"bf16": 2 ** -5, "fp8": 2 ** -4}
+
 
 def ensure_built():
     """The package, with its library built from the current sources (rebuilt
@@ -79,6 +91,21 @@ def assert_close(out, lse, ref_out, ref_lse, kv_dtype, what=""):
     bad = ~(err <= tol)
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} out elements off; max abs err "
                            f"{np.nanmax(err):.4g} at {np.unravel_index(np.nanargmax(err), err.shape)}")
+    # Scale-aware bound per (row, head); heads with no entry (ref all zero)
+    # were checked exactly above.
+    e2 = err.reshape(-1, err.shape[-1])
+    r2 = np.asarray(ref_out, dtype=np.float64).reshape(-1, err.shape[-1])
+    rms = np.sqrt(np.mean(r2 * r2, axis=1))
+    nz = rms > 0
+    ratio = e2.max(axis=1)[nz] / rms[nz] if nz.any() else np.zeros(1)
+    big = np.abs(r2) >= rms[:, None]
+    rel = (np.abs(e2) / np.where(big, np.abs(r2), 1.0))[big & nz[:, None]]
+    print(f"[parity] {what}: max abs err {np.nanmax(err) if err.size else 0.0:.3g}, "
+          f"max rel err (|ref| >= RMS) {rel.max() if rel.size else 0.0:.3g}, "
+          f"max err / RMS per head {ratio.max():.3g} (bound {RMS_TOL[kv_dtype]:.3g})")
+    assert ratio.max() <= RMS_TOL[kv_dtype], (
+        f"{what}: max err / RMS(ref) = {ratio.max():.4g} > {RMS_TOL[kv_dtype]} at (row*head) "
+        f"{np.flatnonzero(nz)[np.argmax(ratio)]}")
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(l), fin), f"{what}: lse finiteness differs"
     assert np.all(np.isneginf(l[~fin])), f"{what}: empty rows must give lse = -inf"

@@ -191,3 +191,48 @@ def test_run_to_run_bitwise(ds):
     b = run_decode(ds, c, idx)
     assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
     assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+
+
+def test_batch_invariance_bitwise_fp8_h128(ds):
+    # The TP1 shape: FP8 KV, 128 heads (two head-group CTAs per split, each
+    # gathering its own copy of every tile), top-k 2048, contexts up to 128K.
+    # One request alone and at random slots of batches of 7 and 64.
+    rng = np.random.default_rng(21)
+    ref = None
+    for B in [1, 7, 64]:
+        for slot in sorted({int(x) for x in rng.integers(0, B, 2)}):
+            c = invariance_batch(B, slot, target_seed=5, batch_seed=6, device="cuda", H=128,
+                                 target_ctx=65536, max_ctx=131072, kv_dtype="fp8")
+            idx = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)
+            out, lse = ds.sparse_mla_decode(c.q, c.kv_pages, "fp8", c.block_table, idx, c.lens,
+                                            c.scale)
+            got = (idx[slot].cpu(), out[slot].cpu(), lse[slot].cpu())
+            if ref is None:
+                ref = got
+                qb, kv, bt, idx_s, lens = compact_rows(c, [slot], idx.cpu().numpy())
+                r_out, r_lse = oracle.sparse_mla_decode(qb, kv, "fp8", bt, idx_s, lens, c.scale)
+                assert_close(out[[slot]], lse[[slot]], r_out, r_lse, "fp8", "fp8 H128 target")
+            assert torch.equal(got[0], ref[0]), (B, slot)
+            assert torch.equal(got[1].view(torch.int16), ref[1].view(torch.int16)), (B, slot)
+            assert torch.equal(got[2].view(torch.int32), ref[2].view(torch.int32)), (B, slot)
+            del c, idx, out, lse
+
+
+def test_prefill_token_alone_equals_token_in_chunk_bitwise(ds):
+    # "Batch-invariant prefill chunks each request independently": a query
+    # token of the 4096-token chunk, run alone (a one-token prefill with the
+    # same block-table row, length and top-k row), gives the same bits.
+    c = workload_case("chunked_prefill", device="cuda")
+    idx = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)
+    del c.scores
+    out, lse = ds.sparse_mla_prefill(c.q, c.kv_pages, c.kv_dtype, c.block_table, c.row_req, idx,
+                                     c.lens, c.scale)
+    torch.cuda.synchronize()
+    tokens = [0, 1, 2047, 4095] + np.random.default_rng(3).choice(4096, 4, replace=False).tolist()
+    for t in tokens:
+        sl = slice(t, t + 1)
+        o1, l1 = ds.sparse_mla_prefill(c.q[sl], c.kv_pages, c.kv_dtype, c.block_table,
+                                       c.row_req[sl], idx[sl], c.lens[sl], c.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0].view(torch.int16), out[t].view(torch.int16)), t
+        assert torch.equal(l1[0].view(torch.int32), lse[t].view(torch.int32)), t

@@ -45,15 +45,50 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
 def test_traffic_record_is_used_only_for_its_own_sources(tmp_path, monkeypatch):
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
         rec = json.load(fh)
-    assert rec["bytes_per_launch"] == rec["split_kernel_bytes"] + rec["combine_kernel_bytes"]
+    for r in rec["records"].values():
+        if "split_kernel_bytes" in r:
+            assert r["bytes_per_launch"] == r["split_kernel_bytes"] + r["combine_kernel_bytes"]
+    key = next(iter(rec["records"]))
+    wl, kern = key.split(":")
     csrc = _copy_csrc(tmp_path)
     (tmp_path / "profiles").mkdir()
     rec["source_sha"] = _sha_at(monkeypatch, tmp_path)
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
-    assert bench.ncu_traffic() == rec
+    assert bench.ncu_traffic(wl, kern) == rec["records"][key]["bytes_per_launch"]
+    assert bench.ncu_traffic(wl, "no_such_kernel") is None
     f = csrc / "combine_note.h"
     f.write_text("#pragma once\nconstexpr int kChanged = 1;\n")
-    assert bench.ncu_traffic() is None
+    assert bench.ncu_traffic(wl, kern) is None
+
+
+def test_warmup_and_steps_are_honoured_exactly():
+    # Replayer runs whole passes over the input sets as one graph and the
+    # rest one set at a time, continuing from where the last call stopped.
+    class G:
+        def __init__(self, log, name):
+            self.log, self.name = log, name
+
+        def replay(self):
+            self.log.append(self.name)
+
+    log = []
+    rep = bench.Replayer.__new__(bench.Replayer)
+    rep.stream, rep.n, rep.pos = None, 4, 0
+    rep.cycle = G(log, "all")
+    rep.single = [G(log, i) for i in range(4)]
+    import contextlib
+    import torch
+    orig = torch.cuda.stream
+    torch.cuda.stream = lambda s: contextlib.nullcontext()
+    try:
+        rep.run(5)      # warm-up of 5 steps
+        assert log == ["all", 0] and rep.pos == 1
+        log.clear()
+        rep.run(20)     # 20 timed steps, continuing at set 1
+        steps = sum(4 if x == "all" else 1 for x in log)
+        assert steps == 20 and log[:3] == [1, 2, 3] and rep.pos == 1
+    finally:
+        torch.cuda.stream = orig
 
 
 def test_e2e_slot_count_is_an_option(monkeypatch):

@@ -57,8 +57,29 @@ def test_single_rank_needs_no_process_group(monkeypatch):
     assert bench.max_over_ranks(3.25, 1) == 3.25
 
 
-@pytest.mark.parametrize("world", [1, 2, 8])
-def test_weak_scaling_value_counts_every_rank(world):
-    # value = rows of all ranks / slowest rank's time.
-    rows, steps, secs = 32, 100, 0.004
-    assert world * rows * steps / secs == pytest.approx(world * 800000.0)
+def _value_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    import torch.distributed as dist
+    r, w, _ = bench.dist_setup(world)
+    # Each rank ran 100 steps of 32 rows in its own time; the job's value
+    # counts every rank's rows over the slowest rank's time.
+    secs = bench.max_over_ranks(0.004 * (1 + r), w)
+    q.put((r, bench.job_value(w, 32, 100, secs)))
+    dist.destroy_process_group()
+
+
+def test_whole_job_value_counts_every_rank_over_the_slowest():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_value_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    # 2 ranks x 32 rows x 100 steps over rank 1's 8 ms.
+    assert got == [(0, pytest.approx(800000.0)), (1, pytest.approx(800000.0))]

@@ -238,3 +238,23 @@ def test_kernel_choice_never_changes_indices(ds):
     for r in [0, 1, 3, 4, 5, 7, 8, 299]:
         one = run(ds, wide[r:r + 1], a[r:r + 1], b[r:r + 1], 2048)[0]
         assert np.array_equal(one, big[r]), r
+
+
+@pytest.mark.parametrize("k", [2048, 8192, 16384])
+def test_rows_wider_than_128k_exact(ds, k):
+    # Rows wider than 131072 scores take the kernel whose histogram passes
+    # read global memory; every refinement case of _mixed_rows on 200003-wide
+    # rows.
+    rng = np.random.default_rng(k + 1)
+    s, a, b = _mixed_rows(rng, 9, 200003, k)
+    check(ds, s, a, b, k)
+
+
+@pytest.mark.parametrize("k", [8192, 16384])
+@pytest.mark.parametrize("rows,stride", [(16, 32768), (256, 40000), (8, 100000)])
+def test_large_k_on_every_kernel_exact(ds, rows, stride, k):
+    # k above 4096 on the whole-row kernel (16 rows of 32K), the streaming
+    # grid (256 rows of 40000) and the cluster kernel (8 rows of 100000).
+    rng = np.random.default_rng(rows * 7 + k)
+    s, a, b = _mixed_rows(rng, rows, stride, k)
+    check(ds, s, a, b, k)

@@ -69,6 +69,8 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row(ds):
         _close(out, lse, want_out, want_lse, c.kv_dtype)
 
 
+@pytest.mark.skipif(torch.cuda.is_available(),
+                    reason="passes fake device addresses; host-validation check only")
 def test_noalloc_rejects_calls_beyond_its_scratch(ds):
     # 128 rows x 128 heads at top-k 2048 need about 134 MB of scratch: refused on
     # the host, before any CUDA call, with a message that says what to use.
