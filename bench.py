@@ -348,9 +348,10 @@ def make_calls(ds, kind, stream):
 
 class Replayer:
     """Runs any number of steps exactly, cycling through the input sets in
-    order: whole passes over the sets replay one CUDA graph of all of them
-    (consecutive steps keep their programmatic-launch overlap), the rest
-    replay one graph per set."""
+    order. A whole pass over the sets replays one CUDA graph of all of them,
+    captured once per starting set (so consecutive steps keep their
+    programmatic-launch overlap wherever a run starts); the rest replay one
+    graph per set."""
 
     def __init__(self, stream, fn, sets):
         import torch
@@ -363,23 +364,21 @@ class Replayer:
                     fn(c)
             return g
 
-        self.cycle = capture(sets)
+        n = len(sets)
+        self.cycles = [capture(sets[k:] + sets[:k]) for k in range(n)]
         self.single = [capture([c]) for c in sets]
-        self.n = len(sets)
+        self.n = n
         self.pos = 0
 
     def run(self, steps):
         import torch
         with torch.cuda.stream(self.stream):   # replay() launches on the current stream
-            i = 0
-            while i < steps:
-                if self.pos == 0 and steps - i >= self.n:
-                    self.cycle.replay()
-                    i += self.n
-                else:
-                    self.single[self.pos].replay()
-                    self.pos = (self.pos + 1) % self.n
-                    i += 1
+            while steps >= self.n:
+                self.cycles[self.pos].replay()
+                steps -= self.n
+            for _ in range(steps):
+                self.single[self.pos].replay()
+                self.pos = (self.pos + 1) % self.n
 
     def timed(self, steps):
         """Seconds for `steps` steps, by CUDA events on the launching stream."""

@@ -67,6 +67,12 @@ constexpr int kSCols = kTile;                         // TMEM columns of one S b
 constexpr int kSbCol = 2 * kSCols;                    // second QK accumulator (2 buffers)
 constexpr int kOCol = 4 * kSCols;                     // first TMEM column of O^T
 constexpr int kMaxSplitTiles = 12;                    // tiles one split may hold
+// Largest split count: top-k 2048 (4 splits of 512), or 2048 + 512 window
+// entries at most 768 per split (4).
+constexpr int kMaxSplits = 4;
+static_assert((2048 + kSplitEntries - 1) / kSplitEntries <= kMaxSplits &&
+                  (2048 + 512 + 767) / 768 <= kMaxSplits,
+              "every split of the largest call is merged");
 constexpr int kQkSplitAtom = 5;                       // QK column blocks [0,5) -> S_a, [5,9) -> S_b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 // P(t) is written over the rope column block of tile t's own stage: QK(t) is
@@ -75,27 +81,37 @@ constexpr float kRescaleThreshold = 8.0f;             // log2 units
 // the stages at no cost in shared memory.
 constexpr int kPAtom = 8 * kAtomStride;
 
-// Warp roles. Warps 0-3 run the softmax; warps 4-11 load; then come one QK
-// issuer, the PV issuer and the second QK issuer. Loader warp pw fills rows
-// kRowsPerWarp * pw .. + kRowsPerWarp - 1 of every tile; for the page
-// lookups, lane l owns row kRowsPerWarp * pw + (l % kRowsPerWarp) of tiles
-// l / kRowsPerWarp + kTileGroups * i, i = 0 .. kSlots - 1.
+// Warp roles. Warps 0-3 run the softmax (warp w reads the TMEM lane
+// quadrant w, i.e. heads 16 w .. 16 w + 15); the next kLoaderWarps warps
+// load; then come one QK issuer, the PV issuer and the second QK issuer.
+// Loader warp pw fills rows kRowsPerWarp * pw .. + kRowsPerWarp - 1 of every
+// tile; for the page lookups, lane l owns row kRowsPerWarp * pw +
+// (l % kRowsPerWarp) of tiles l / kRowsPerWarp + kTileGroups * i,
+// i = 0 .. kSlots - 1. (Eight softmax warps, or four loader warps, were
+// measured no faster.)
 template <bool FP8>
 struct Roles {
+  static constexpr int kSoftmaxWarps = 4;
+  static constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
   static constexpr int kLoaderWarps = 8;
   static constexpr int kLoaderThreads = 32 * kLoaderWarps;
-  static constexpr int kRowsPerWarp = 64 / kLoaderWarps;          // 8
-  static constexpr int kTileGroups = 32 / kRowsPerWarp;           // 4
-  static constexpr int kSlots = kMaxSplitTiles / kTileGroups;    // 3
-  static constexpr int kQkA = 4 + kLoaderWarps;                   // also allocates TMEM
+  static constexpr int kRowsPerWarp = 64 / kLoaderWarps;
+  static constexpr int kTileGroups = 32 / kRowsPerWarp;
+  static constexpr int kSlots = kMaxSplitTiles / kTileGroups;
+  static constexpr int kQkA = kSoftmaxWarps + kLoaderWarps;       // also allocates TMEM
   static constexpr int kPv = kQkA + 1;
   static constexpr int kQkB = kQkA + 2;
-  static constexpr int kThreads = 32 * (kQkA + 3);                // 480
+  static constexpr int kThreads = 32 * (kQkA + 3);
+  static_assert(kLoaderWarps == 4 || kLoaderWarps == 8, "loader warps");
 };
 
 // The loader lane's KV row of slot `sel` (select chain: no local memory).
-__device__ __forceinline__ int slot_row(const int (&grow)[4], int sel) {
-  return sel == 0 ? grow[0] : sel == 1 ? grow[1] : sel == 2 ? grow[2] : grow[3];
+template <int N>
+__device__ __forceinline__ int slot_row(const int (&grow)[N], int sel) {
+  int r = grow[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) r = sel == i ? grow[i] : r;
+  return r;
 }
 
 // Error bits (match DS_DEVERR_* in the public header).
@@ -135,11 +151,75 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// ---- The fixed-order merge of one (row, head)'s splits (A9), in log2 units
+// (the sink logit s enters as s log2 e):
+// M = max(m_s, sink), L = sum 2^(m_s - M) l_s + 2^(sink - M),
+// out = sum 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2, splits in order
+// s = 0, 1, ...; a split with m = -inf is empty and skipped (its O is never
+// read); a NaN m (a split that gave up on a wait) makes the result NaN.
+struct MergeWeights {
+  float w[kMaxSplits];   // 2^(m_s - M); 0 for skipped splits
+  float inv;             // 1 / L
+  float lse;             // natural log
+  uint32_t skip;         // bit s: split s is empty
+  int state;             // 0: merged; 1: no entry (out 0, lse -inf); 2: gave up (NaN)
+};
+
+__device__ __forceinline__ MergeWeights merge_weights(const float (&ms)[kMaxSplits],
+                                                      const float (&ls)[kMaxSplits], float sl) {
+  MergeWeights r;
+  float M = sl;
+  bool gave_up = false;
+  r.skip = 0u;
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) {
+    M = fmaxf(M, ms[s]);
+    gave_up |= ms[s] != ms[s];
+    r.w[s] = 0.0f;
+    if (ms[s] == -INFINITY) r.skip |= 1u << s;
+  }
+  r.inv = 0.0f;
+  r.lse = -INFINITY;
+  r.state = gave_up ? 2 : (M == -INFINITY ? 1 : 0);
+  if (r.state != 0) return r;
+  float L = 0.0f;
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) {
+    if ((r.skip >> s) & 1u) continue;
+    r.w[s] = ex2(ms[s] - M);
+    L = __fmaf_rn(r.w[s], ls[s], L);
+  }
+  if (sl != -INFINITY) L = __fadd_rn(L, ex2(sl - M));
+  r.inv = __fdiv_rn(1.0f, L);
+  r.lse = __fmul_rn(__fadd_rn(M, log2f(L)), 0.69314718055994530942f);
+  return r;
+}
+
+// One output element from the splits' unnormalised partial values o[s].
+__device__ __forceinline__ float merge_value(const MergeWeights& mw, const float (&o)[kMaxSplits]) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s)
+    if (!((mw.skip >> s) & 1u)) acc = __fmaf_rn(mw.w[s], o[s], acc);
+  return __fmul_rn(acc, mw.inv);
+}
+
 // Byte offset of 16-byte chunk `c` (of 72) of tile row `r` in a 128-byte
 // swizzled K-major tile whose 64-dim column blocks are `atom_stride` apart.
 __device__ __forceinline__ uint32_t swz_off(int r, int c, int atom_stride) {
   return (uint32_t)((c >> 3) * atom_stride + (r >> 3) * 1024 + (r & 7) * 128 +
                     (((c & 7) ^ (r & 7)) << 4));
+}
+
+// N (16, 32 or 64) consecutive TMEM columns of this warp's lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
+  if constexpr (N == 64)
+    tmem_ld64_sync(taddr, v);
+  else if constexpr (N == 32)
+    tmem_ld32_sync(taddr, v);
+  else
+    tmem_ld16_sync(taddr, v);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -177,8 +257,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// Starts an asynchronous copy of `bytes` (a multiple of 16, 16-byte aligned
-// source) from global memory into L2, without waiting for it.
 // Requests every 128-byte line of [base, base + bytes) into L2 (or into this
 // SM's L1), thread `first` of `step` threads taking every step-th line. A
 // line that holds a byte of the range lies in a mapped page, so no request
@@ -195,10 +273,6 @@ __device__ __forceinline__ void prefetch_lines(const void* base, int64_t bytes, 
     else
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
   }
-}
-
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 struct KParams {
@@ -237,6 +311,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   using LY = Layout<HG>;
   using RL = Roles<FP8>;
   constexpr int RW = RL::kRowsPerWarp, TG = RL::kTileGroups;
+  constexpr int SWT = RL::kSoftmaxThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -252,8 +327,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   const int lane = tid & 31;
   // The loader warps load every KV tile together (see Roles); the softmax
   // warps copy Q.
-  const bool producer = warp >= 4 && warp < 4 + RL::kLoaderWarps;
-  const int pw = warp - 4;
+  const bool producer = warp >= RL::kSoftmaxWarps && warp < RL::kSoftmaxWarps + RL::kLoaderWarps;
+  const int pw = warp - RL::kSoftmaxWarps;
   const int lgroup = lane / RW, lrow = lane % RW;   // tile group and row of this lane
 
   int64_t bid = blockIdx.x;
@@ -275,8 +350,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       // loader thread; s_full: one tcgen05.commit from each QK issuer; the
       // rest: one tcgen05.commit.
       uint32_t count = 1u;
-      if (i == kPFull || i == kPFull + 1) count = 128u;
-      if (i == kQFull) count = 128u;
+      if (i == kPFull || i == kPFull + 1) count = (uint32_t)SWT;
+      if (i == kQFull) count = (uint32_t)SWT;
       if (i >= kKvFull && i < kKvFull + kStages) count = RL::kLoaderThreads;
       if (i == kSFull || i == kSFull + 1) count = 2u;
       mbar_init(&bars[i], count);
@@ -298,9 +373,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   const int ntiles = (int)((int64_t)(split + 1) * T / p.num_splits) - u0;
   if (producer) {
     prefetch_lines<false>(p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD,
-                          HG * kRowBytesBf16, tid - 128, RL::kLoaderThreads);
+                          HG * kRowBytesBf16, tid - SWT, RL::kLoaderThreads);
     if (p.row_req == nullptr)
-      prefetch_lines<false>(p.block_table + row * p.bt_stride, p.bt_stride * 4, tid - 128,
+      prefetch_lines<false>(p.block_table + row * p.bt_stride, p.bt_stride * 4, tid - SWT,
                             RL::kLoaderThreads);
     // The split's top-k entries, usually written by the kernel still running
     // ahead of this one: the request warms L2 and this SM's address
@@ -308,8 +383,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     const int u_end = min(u0 + ntiles, T1);
     if (u_end > u0)
       prefetch_lines<false>(p.idx + row * (int64_t)p.k + u0 * kTile,
-                            (int64_t)(u_end - u0) * kTile * 4, tid - 128, RL::kLoaderThreads);
-    prefetch_lines<false>(p.lens + row, 4, tid - 128, RL::kLoaderThreads);
+                            (int64_t)(u_end - u0) * kTile * 4, tid - SWT, RL::kLoaderThreads);
+    prefetch_lines<false>(p.lens + row, 4, tid - SWT, RL::kLoaderThreads);
   }
   pdl_wait();
   pdl_trigger();
@@ -333,12 +408,12 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   // entries, resolve pages and start the tile 0 and 1 copies; the softmax
   // warps copy Q.
   __syncthreads();   // barriers, TMEM and neff_s = 0 are visible before use
-  if (tid < 128) {
+  if (tid < SWT) {
     // The softmax warps have nothing to do until the first S: they copy Q
     // (requested into L2 before the wait) while the loaders look up entries,
     // so Q's copies never queue ahead of a KV tile's.
     const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
-    for (int c = tid; c < HG * kChunks; c += 128) {
+    for (int c = tid; c < HG * kChunks; c += SWT) {
       const int h = c / kChunks, ch = c - h * kChunks;
       cp_async_16(sbase + LY::kQ + swz_off(h, ch, HG * 128), qg + (int64_t)h * kD + ch * 8, 16);
     }
@@ -347,7 +422,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   }
   // KV row (page * 64 + slot) of each owned entry, -1 = skip: slot i is
   // tile lgroup + TG i, row RW pw + lrow.
-  int grow[4] = {-1, -1, -1, -1};
+  int grow[RL::kSlots];
+#pragma unroll
+  for (int i = 0; i < RL::kSlots; ++i) grow[i] = -1;
   // bf16 pools: loader warp pw copies rows RW pw .. RW pw + RW - 1 of tile t
   // into the stage at stage_base, 16-byte cp.async into the 128-byte
   // swizzled layout; entries that are not valid copy zeros.
@@ -369,8 +446,13 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     cp_async_commit();
   };
   if (producer) {
-    int pos[4] = {-1, -1, -1, -1};
-    bool sec[4] = {false, false, false, false};   // slot's tile is in the second list
+    int pos[RL::kSlots];
+    bool sec[RL::kSlots];   // slot's tile is in the second list
+#pragma unroll
+    for (int i = 0; i < RL::kSlots; ++i) {
+      pos[i] = -1;
+      sec[i] = false;
+    }
     int last = 0;
 #pragma unroll
     for (int i = 0; i < RL::kSlots; ++i) {
@@ -387,17 +469,17 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     // is cached): the page lookups below then hit L1 instead of making a
     // second round trip to L2.
     if (row_ok) {
-      prefetch_lines<true>(p.block_table + bt_row * p.bt_stride, p.bt_stride * 4, tid - 128,
+      prefetch_lines<true>(p.block_table + bt_row * p.bt_stride, p.bt_stride * 4, tid - SWT,
                            RL::kLoaderThreads);
       if (p.k2 > 0)
         prefetch_lines<true>(p.block_table2 + bt_row * p.bt_stride2, p.bt_stride2 * 4,
-                             tid - 128, RL::kLoaderThreads);
+                             tid - SWT, RL::kLoaderThreads);
     }
 #pragma unroll
     for (int i = 0; i < RL::kSlots; ++i)
       if (pos[i] != -1) last = lgroup + TG * i + 1;
     // All block-table reads go out before any is used: one round trip.
-    int64_t page[4];
+    int64_t page[RL::kSlots];
 #pragma unroll
     for (int i = 0; i < RL::kSlots; ++i) {
       const int ps = pos[i];
@@ -437,29 +519,17 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
         }
       }
     }
-    // Start tile 0 (stage 0) and tile 1 (stage 1), and stream tiles 2 and 3
-    // into L2 right away, before the block-wide barrier, in the order they
-    // are needed: every CTA starts at once, so requests issued later queue
-    // behind earlier ones at HBM. Entries that are not valid copy zeros, so
-    // this is harmless when the split turns out to be short.
-    {
-      const int row_bytes = FP8 ? kRowBytesFp8 : kRowBytesBf16;
-      // Each arrival tracks every earlier copy of the thread, so tile 0
-      // signals its barrier before tile 1 is issued.
-      if constexpr (!FP8) {
-        copy_tile_bf16(0, sbase + LY::kKV);
-        cp_async_mbar_arrive_noinc(&bars[kKvFull]);
-      }
-      if (!FP8 && ntiles > 1) {   // a one-tile split has no tile 1 (nor its pool)
+    // Start tile 0 (stage 0) and tile 1 (stage 1) right away, before the
+    // block-wide barrier. Entries that are not valid copy zeros, so this is
+    // harmless when the split turns out to be short. Each arrival tracks
+    // every earlier copy of the thread, so tile 0 signals its barrier before
+    // tile 1 is issued.
+    if constexpr (!FP8) {
+      copy_tile_bf16(0, sbase + LY::kKV);
+      cp_async_mbar_arrive_noinc(&bars[kKvFull]);
+      if (ntiles > 1) {   // a one-tile split has no tile 1 (nor its pool)
         copy_tile_bf16(1, sbase + LY::kKV + kStageBytes);
         cp_async_mbar_arrive_noinc(&bars[kKvFull + 1]);
-      }
-#pragma unroll
-      for (int u = 2; u < 4; ++u) {   // tiles 2 and 3
-        if (u < ntiles && lgroup == u % TG) {
-          const int g = slot_row(grow, u / TG);
-          if (g >= 0) prefetch_l2_bulk(tile_kv(u) + (int64_t)g * row_bytes, (uint32_t)row_bytes);
-        }
       }
     }
 #pragma unroll
@@ -477,7 +547,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   bool failed = false;
   if (n_eff == 0) {
     // Nothing to attend to in this split: an empty partial.
-    if (producer || tid < 128) cp_async_wait_all();  // copies land before the CTA exits
+    if (producer || tid < SWT) cp_async_wait_all();  // copies land before the CTA exits
     if (tid < HG) {
       p.part_m[part_base + tid] = -INFINITY;
       p.part_l[part_base + tid] = 0.0f;
@@ -489,22 +559,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     // land (cp.async.mbarrier.arrive), so a loader moves on to the next stage
     // as soon as it is free and up to two tiles are in flight; the tensor-core
     // issuers fence the landed tiles for the async proxy. FP8: the loaders
-    // dequantise through registers, store, fence and arrive. Shared memory
-    // holds only two tiles, so L2 serves as the deeper stages: while tile t is
-    // copied, the rows of tile t + 3 are streamed into L2 with bulk
-    // prefetches (tiles 2 and 3 at the start), in tile order, so each tile's
-    // HBM reads overlap the compute of the tiles before it and its smem
-    // copies hit L2.
+    // dequantise through registers, store, fence and arrive. Nothing is
+    // requested into L2 ahead of the copies: measured on this gather
+    // pattern, bulk or per-line L2 prefetches of later tiles slowed the
+    // tile fills down rather than hiding their latency.
     // Rows of tile u are held by lanes with lgroup == u % TG, slot u / TG.
-    auto prefetch_tile = [&](int u, int row_bytes) {
-      if (u < n_eff && lgroup == u % TG) {
-        const int g = slot_row(grow, u / TG);
-        if (g >= 0) prefetch_l2_bulk(tile_kv(u) + (int64_t)g * row_bytes, (uint32_t)row_bytes);
-      }
-    };
-    auto prefetch_ahead = [&](int t, int row_bytes) {
-      if (t >= 1) prefetch_tile(t + 3, row_bytes);   // tiles 2 and 3 went out in the prologue
-    };
 #pragma unroll 1
     for (int t = 0; t < n_eff; ++t) {
       const int stage = t & 1;
@@ -519,11 +578,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
           copy_tile_bf16(t, stage_base);
           cp_async_mbar_arrive_noinc(&bars[kKvFull + stage]);
         }
-        prefetch_ahead(t, kRowBytesBf16);
       } else {
         const int gi = slot_row(grow, t / TG);
         const int src_lane0 = (t % TG) * RW;
-        prefetch_ahead(t, kRowBytesFp8);
 #pragma unroll 1
         for (int r0 = 0; r0 < RW; r0 += 8) {
           uint2 codes[8][2];
@@ -642,64 +699,70 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       mbar_wait(&bars[kMmaDone + 1], 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < RL::kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax
     // S was computed with M = 64: head h sits in TMEM lane 32*(h/16) + h%16,
-    // so every softmax warp holds 16 heads (its lanes 0-15). With the
-    // 16x32bx2 load, lane l and lane l+16 both read head 16*warp + l%16:
-    // entries 0-31 and 32-63 of the tile respectively. Row max and sum are
-    // combined between the two with one shuffle.
+    // so warp qd holds heads 16 qd .. 16 qd + 15 (its lanes 0-15). With the
+    // 16x32bx2 load, lane l and lane l + 16 both read head 16 qd + l % 16:
+    // entries 0-31 and 32-63 of the tile. A head's max and sum are combined
+    // between the two halves with one shuffle.
+    constexpr int NE = kTile / 2;   // entries per thread
+    const int qd = warp;
     const int hl = lane & 15;
     const int half = lane >> 4;
-    const int h = warp * 16 + hl;
+    const int h = qd * 16 + hl;
     const bool active = h < HG;
-    const bool warp_has_heads = warp * 16 < HG;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const bool warp_has_heads = qd * 16 < HG;
+    const int e0 = half * NE;   // first entry of this thread
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t prow = sbase + LY::kKV + kPAtom + (h >> 3) * 1024 + (h & 7) * 128;
-    float m = -INFINITY, l = 0.0f;   // l: this half's share of the row sum
-    float s[32];
-    // The four softmax warps meet at named barriers (ids 1-2), so every
-    // timeout decision is made jointly: either all leave the loop or none.
+    float m = -INFINITY, l = 0.0f;   // l: this thread's share of the row sum
+    float s[NE];
+    // The softmax warps meet at named barriers (ids 1-2), so every timeout
+    // decision is made jointly: either all leave the loop or none.
     for (int t = 0; t < n_eff; ++t) {
       const int sb = t & 1;
       bool ok = mbar_wait(&bars[kSFull + sb], (t >> 1) & 1);
       bool need = false;
+      float mt = -INFINITY;
       if (ok) {
         tc_fence_after();
         if (warp_has_heads) {
-          float s2[32];
-          tmem_ld16x32bx2_x32_pair_sync(tmem + lane_base + sb * kSCols,
-                                        tmem + lane_base + kSbCol + sb * kSCols, s, s2);
+          float s2[NE];
+          const uint32_t col = (uint32_t)(sb * kSCols);
+          tmem_ld16x32bx2_x32_pair_sync(tmem + lane_base + col, tmem + lane_base + kSbCol + col, s,
+                                        s2);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) s[j] += s2[j];
-          const uint32_t mask = vmask[2 * t + half];
-          float mt = -INFINITY;
+          for (int j = 0; j < NE; ++j) s[j] += s2[j];
+          const uint32_t mask = vmask[2 * t + (e0 >> 5)] >> (e0 & 31);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < NE; ++j) {
             s[j] = ((mask >> j) & 1u) ? s[j] * p.scale_log2 : -INFINITY;
             mt = fmaxf(mt, s[j]);
           }
           mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-          float a = 1.0f;
-          if (mt > m + kRescaleThreshold) {
-            a = (m == -INFINITY) ? 0.0f : ex2(m - mt);
-            need = t > 0;
-            l *= a;
-            m = mt;
-          }
-          if (active && half == 0) alpha_s[sb * 64 + h] = a;
         }
       }
-      if (named_bar_or(1, 128, !ok)) {
+      if (named_bar_or(1, SWT, !ok)) {
         failed = true;
         break;
       }
-      const bool any = named_bar_or(2, 128, need && active);
+      if (warp_has_heads) {
+        float a = 1.0f;
+        if (mt > m + kRescaleThreshold) {
+          a = (m == -INFINITY) ? 0.0f : ex2(m - mt);
+          need = t > 0;
+          l *= a;
+          m = mt;
+        }
+        if (active && half == 0) alpha_s[sb * 64 + h] = a;
+      }
+      const bool any = named_bar_or(2, SWT, need && active);
       tc_fence_after();
       if (active) {
         float lsum = 0.0f;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c4 = 0; c4 < NE / 8; ++c4) {
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -711,7 +774,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
             lsum += pr.y;
             w[i] = *reinterpret_cast<const uint32_t*>(&pb);
           }
-          const int c8 = 4 * half + c4;   // 16-byte chunk of the 128-byte P row
+          const int c8 = (e0 >> 3) + c4;   // 16-byte chunk of the 128-byte P row
           st_shared_v4(prow + sb * kStageBytes + ((c8 ^ (h & 7)) << 4),
                        make_uint4(w[0], w[1], w[2], w[3]));
         }
@@ -722,7 +785,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
         // PV(t-2) completed, so the stage barrier of PV(t-1) is at most one
         // phase from it and its parity test is exact.
         const bool pv_ok = mbar_wait(&bars[kKvEmpty + ((t - 1) & 1)], ((t - 1) >> 1) & 1);
-        if (named_bar_or(1, 128, !pv_ok)) {
+        if (named_bar_or(1, SWT, !pv_ok)) {
           failed = true;
           break;
         }
@@ -746,36 +809,32 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       tc_fence_before();
       mbar_arrive(&bars[kPFull + sb]);
     }
-    if (!failed && !mbar_wait(&bars[kKvEmpty + ((n_eff - 1) & 1)], ((n_eff - 1) >> 1) & 1))
-      failed = true;
+    if (!failed) {
+      const bool pv_ok =
+          mbar_wait(&bars[kKvEmpty + ((n_eff - 1) & 1)], ((n_eff - 1) >> 1) & 1);
+      failed = named_bar_or(1, SWT, !pv_ok);   // a joint decision
+    }
     if (!failed) {
       tc_fence_after();
       // Epilogue: partial O (unnormalised, relative to m), m and l.
-      const int dv_lane = warp * 32 + lane;
+      const int dv_lane = qd * 32 + lane;
       float* po = p.part_o + part_base * kDv;
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
         float v[HG];
-        const uint32_t addr = tmem + lane_base + kOCol + b * HG;
-        if constexpr (HG == 64) {
-          tmem_ld64_sync(addr, v);
-        } else if constexpr (HG == 32) {
-          tmem_ld32_sync(addr, v);
-        } else {
-          tmem_ld16_sync(addr, v);
-        }
+        tmem_ld_cols<HG>(tmem + lane_base + kOCol + b * HG, v);
 #pragma unroll
         for (int i = 0; i < HG; ++i) po[(int64_t)i * kDv + 128 * b + dv_lane] = v[i];
       }
-      const float l_other = __shfl_xor_sync(0xffffffffu, l, 16);
+      const float lw = l + __shfl_xor_sync(0xffffffffu, l, 16);
       if (active && half == 0) {
         p.part_m[part_base + h] = m;
-        p.part_l[part_base + h] = l + l_other;
+        p.part_l[part_base + h] = lw;
       }
     }
   }
 
-  if (tid < 128) cp_async_wait_all();   // Q copies, on every path
+  if (tid < SWT) cp_async_wait_all();   // Q copies, on every path
   if (failed && p.err != nullptr) atomicOr(p.err, kErrTimeout);
   tc_fence_before();
   const bool cta_failed = __syncthreads_or(failed);
@@ -789,19 +848,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   if (warp == RL::kQkA) tmem_dealloc(tmem, LY::kTmemCols);
 }
 
-// Merges the splits of one (row, head) in split order: M = max(m_s, sink),
-// L = sum 2^(m_s - M) l_s + 2^(sink - M), out = sum 2^(m_s - M) O_s / L,
-// lse = (M + log2 L) ln 2, all in log2 units (the sink logit s becomes
-// s log2 e). The sink joins the denominator only, after the splits, and -inf
-// (or no sink array) leaves the sum as it is. Every split's m, l and O slice
-// is loaded in one round (at most kMaxSplits) before any arithmetic.
-// Largest split count: top-k 2048 (4 splits of 512), or 2048 + 512 window
-// entries at most 768 per split (4).
-constexpr int kMaxSplits = 4;
-static_assert((2048 + kSplitEntries - 1) / kSplitEntries <= kMaxSplits &&
-                  (2048 + 512 + 767) / 768 <= kMaxSplits,
-              "every split of the largest call is merged");
-
+// Merges the splits of one (row, head) in split order (merge_weights,
+// merge_value), reading the partial results from the workspace. Every split's
+// m, l and O slice is loaded in one round before any arithmetic.
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
                                                       const float* __restrict__ part_m,
                                                       const float* __restrict__ part_l,
@@ -828,43 +877,34 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     }
   }
   const float sl = sink != nullptr ? sink[rh % H] * 1.4426950408889634f : -INFINITY;
-  float M = sl;
-  bool gave_up = false;   // a split that timed out left NaN partials
-#pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) {
-    M = fmaxf(M, ms[s]);
-    gave_up |= ms[s] != ms[s];
-  }
+  const MergeWeights mw = merge_weights(ms, ls, sl);
   __nv_bfloat16* o = out + rh * kDv + 4 * t;
-  if (gave_up) {
+  if (mw.state == 2) {   // a split that timed out left NaN partials
     *reinterpret_cast<uint2*>(o) = make_uint2(0x7fc07fc0u, 0x7fc07fc0u);
     if (t == 0) lse[rh] = __int_as_float(0x7fc00000);
     return;
   }
-  if (M == -INFINITY) {
+  if (mw.state == 1) {
     *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
     if (t == 0) lse[rh] = -INFINITY;
     return;
   }
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float L = 0.0f;
-#pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) {
-    if (ms[s] == -INFINITY) continue;   // empty split (its O slice is never read)
-    const float w = ex2(ms[s] - M);
-    L += w * ls[s];
-    acc[0] += w * os[s].x;
-    acc[1] += w * os[s].y;
-    acc[2] += w * os[s].z;
-    acc[3] += w * os[s].w;
+  float v[4];
+  {
+    const float o0[kMaxSplits] = {os[0].x, os[1].x, os[2].x, os[3].x};
+    const float o1[kMaxSplits] = {os[0].y, os[1].y, os[2].y, os[3].y};
+    const float o2[kMaxSplits] = {os[0].z, os[1].z, os[2].z, os[3].z};
+    const float o3[kMaxSplits] = {os[0].w, os[1].w, os[2].w, os[3].w};
+    v[0] = merge_value(mw, o0);
+    v[1] = merge_value(mw, o1);
+    v[2] = merge_value(mw, o2);
+    v[3] = merge_value(mw, o3);
   }
-  if (sl != -INFINITY) L += ex2(sl - M);
-  const float inv = 1.0f / L;
   uint2 r;
-  r.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  r.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  r.x = pack_bf16x2(v[0], v[1]);
+  r.y = pack_bf16x2(v[2], v[3]);
   *reinterpret_cast<uint2*>(o) = r;
-  if (t == 0) lse[rh] = (M + log2f(L)) * 0.69314718055994530942f;
+  if (t == 0) lse[rh] = mw.lse;
 }
 
 template <int HG, bool FP8>

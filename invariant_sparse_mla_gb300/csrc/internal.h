@@ -124,11 +124,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // returns `status`.
 int report_error(int status, const char* fmt, ...);
 
-// The device a launch on `stream` runs on: the stream's own device, or the
-// current device for the legacy default stream.
-inline cudaError_t stream_device(cudaStream_t stream, int* dev) {
-  if (stream == nullptr) return cudaGetDevice(dev);
-  return cudaStreamGetDevice(stream, dev);
+// The device a launch on `stream` runs on. The runtime launches only into a
+// stream of the current device (a stream of another device is refused), so
+// this is the current device; the stream is not queried, since querying a
+// stream is not allowed while it is being captured into a CUDA graph.
+inline cudaError_t stream_device(cudaStream_t /*stream*/, int* dev) {
+  return cudaGetDevice(dev);
 }
 
 // A kernel attribute (the dynamic shared memory limit) is a per-device

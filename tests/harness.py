@@ -98,8 +98,8 @@ def assert_close(out, lse, ref_out, ref_lse, kv_dtype, what=""):
     rms = np.sqrt(np.mean(r2 * r2, axis=1))
     nz = rms > 0
     ratio = e2.max(axis=1)[nz] / rms[nz] if nz.any() else np.zeros(1)
-    big = np.abs(r2) >= rms[:, None]
-    rel = (np.abs(e2) / np.where(big, np.abs(r2), 1.0))[big & nz[:, None]]
+    big = (np.abs(r2) >= rms[:, None]) & nz[:, None]
+    rel = (np.abs(e2) / np.where(big, np.abs(r2), 1.0))[big]
     print(f"[parity] {what}: max abs err {np.nanmax(err) if err.size else 0.0:.3g}, "
           f"max rel err (|ref| >= RMS) {rel.max() if rel.size else 0.0:.3g}, "
           f"max err / RMS per head {ratio.max():.3g} (bound {RMS_TOL[kv_dtype]:.3g})")

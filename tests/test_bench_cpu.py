@@ -62,8 +62,9 @@ def test_traffic_record_is_used_only_for_its_own_sources(tmp_path, monkeypatch):
 
 
 def test_warmup_and_steps_are_honoured_exactly():
-    # Replayer runs whole passes over the input sets as one graph and the
-    # rest one set at a time, continuing from where the last call stopped.
+    # Replayer runs whole passes over the input sets as one graph (captured
+    # once per starting set) and the rest one set at a time, continuing from
+    # where the last call stopped.
     class G:
         def __init__(self, log, name):
             self.log, self.name = log, name
@@ -74,7 +75,7 @@ def test_warmup_and_steps_are_honoured_exactly():
     log = []
     rep = bench.Replayer.__new__(bench.Replayer)
     rep.stream, rep.n, rep.pos = None, 4, 0
-    rep.cycle = G(log, "all")
+    rep.cycles = [G(log, f"all@{k}") for k in range(4)]
     rep.single = [G(log, i) for i in range(4)]
     import contextlib
     import torch
@@ -82,20 +83,12 @@ def test_warmup_and_steps_are_honoured_exactly():
     torch.cuda.stream = lambda s: contextlib.nullcontext()
     try:
         rep.run(5)      # warm-up of 5 steps
-        assert log == ["all", 0] and rep.pos == 1
+        assert log == ["all@0", 0] and rep.pos == 1
         log.clear()
-        rep.run(20)     # 20 timed steps, continuing at set 1
-        steps = sum(4 if x == "all" else 1 for x in log)
-        assert steps == 20 and log[:3] == [1, 2, 3] and rep.pos == 1
+        rep.run(20)     # 20 timed steps, continuing at set 1: five whole passes
+        assert log == ["all@1"] * 5 and rep.pos == 1
+        log.clear()
+        rep.run(6)
+        assert log == ["all@1", 1, 2] and rep.pos == 3
     finally:
         torch.cuda.stream = orig
-
-
-def test_e2e_slot_count_is_an_option(monkeypatch):
-    monkeypatch.setattr("sys.argv", ["bench.py"])
-    assert bench.parse_args().e2e_slots == bench.E2E_SLOTS
-    monkeypatch.setattr("sys.argv", ["bench.py", "--e2e-slots", "2"])
-    assert bench.parse_args().e2e_slots == 2
-    monkeypatch.setattr("sys.argv", ["bench.py", "--e2e-slots", "0"])
-    with pytest.raises(SystemExit):
-        bench.parse_args()
