@@ -17,6 +17,9 @@ Each function cites the passage of the source pages it follows:
   DSpark" (vllm-project/vllm PR 51538), section "What is fixed".
 * "[JJ] Preallocate DeepSeek V4 padded-query output" (local-inference-lab/vllm
   PR 671), section "Operation contract" (caller-owned outputs).
+* "[SM120] Sync DS4 with upstream main + validated perf backports" (jasl/vllm
+  PR 47), which names the indexer's MQA logits; their formula is the
+  DeepSeek-V3.2-Exp lightning indexer (outside the pages; see indexer.py).
 
 Where the pages are silent the oracle takes one plain reading and states it
 in the function's docstring.
@@ -35,6 +38,7 @@ from .fp8 import (  # noqa: F401
     quantize_latent_rows,
     kv_cache_write,
 )
+from .indexer import indexer_logits, indexer_row_length  # noqa: F401
 from .attention import (  # noqa: F401
     gather_latent_rows,
     sparse_mla_rows,
