@@ -460,6 +460,63 @@ def measure_extra(ds, wl, dev, stream, steps, warmup):
     return res
 
 
+def measure_indexer(ds, dev, stream, steps, warmup):
+    """The indexer in front of the TP2 decode batch: its logits (MQA scores
+    over the paged bf16 key cache, 64 heads x 128 dims) and the top-k 2048
+    over them, replayed from CUDA graphs. Roofline of the logits kernel
+    against HBM: every key row read once, q and w read, logits written."""
+    import torch
+    from synthetic import indexer_workload, INDEXER_WORKLOADS
+    w = INDEXER_WORKLOADS["tp2_indexer"]
+    c = indexer_workload("tp2_indexer", device=dev)
+    R, H = c.q.shape[0], c.q.shape[1]
+    logits = torch.empty((R, 64 * c.block_table.shape[1]), dtype=torch.float32, device=dev)
+    idx = torch.empty((R, w["k"]), dtype=torch.int32, device=dev)
+    starts = torch.zeros_like(c.lens)
+
+    def lg(_):
+        ds.indexer_logits(c.q, c.w, c.k_pages, c.block_table, c.lens, logits=logits, stream=stream)
+
+    def tk(_):
+        ds.topk_per_row(logits, starts, c.lens, w["k"], idx_out=idx, stream=stream)
+
+    def step(x):
+        lg(x)
+        tk(x)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step(None)
+    stream.synchronize()
+    rs, rl, rt = (Replayer(stream, f, [None]) for f in (step, lg, tk))
+    rs.run(warmup)
+    secs = rs.timed(steps)
+    lg_s = per_call_seconds(rl, steps)
+    tk_s = per_call_seconds(rt, steps)
+    positions = int(c.lens.clamp(min=0).sum())
+    key_bytes = positions * 128 * 2
+    lg_bytes = key_bytes + c.q.numel() * 2 + c.w.numel() * 4 + positions * 4
+    lg_flops = 2 * H * 128 * positions
+    tk_bytes = positions * 4 + idx.numel() * 4
+    hbm, tflops, peak_kind = load_peaks()
+    res = {"workload": ("indexer logits (64 heads x 128 dims, bf16 paged keys, fp32 head weights) "
+                        "then top-k 2048, over the TP2 decode batch's 32 rows of contexts "
+                        "uniform in [4096, 32768]"),
+           "rows": R, "heads": H, "positions": positions, "steps": steps, "warmup": warmup,
+           "step_us": round(secs / steps * 1e6, 3), "rows_per_s": round(R * steps / secs, 1),
+           "logits_us": round(lg_s * 1e6, 3), "topk_us": round(tk_s * 1e6, 3),
+           "roofline": roofline_block("hbm", lg_bytes, lg_s, hbm, tflops, peak_kind,
+                                      "indexer_kernel", ncu_traffic("tp2_indexer", "logits")),
+           "logits_tflops": round(lg_flops / lg_s / 1e12, 1),
+           "roofline_topk": roofline_block("hbm", tk_bytes, tk_s, hbm, tflops, peak_kind,
+                                           "ds_topk_per_row", None),
+           "l2": f"one input set; {key_bytes / 1e6:.0f} MB of keys per step vs 129 MB L2"}
+    del rs, rl, rt, c, logits, idx
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 EXTRA_WORKLOADS = ("tp1_fp8_decode", "chunked_prefill")
 
 
@@ -576,6 +633,7 @@ def run_ours(args, rank, world, local):
         torch.cuda.empty_cache()
         line["other_configs"] = {x: measure_extra(ds, x, dev, stream, EXTRA_STEPS[x], 3)
                                  for x in EXTRA_WORKLOADS}
+        line["other_configs"]["tp2_indexer_topk"] = measure_indexer(ds, dev, stream, 200, 3)
     return line
 
 

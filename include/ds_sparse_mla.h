@@ -87,6 +87,7 @@ typedef enum {
 #define DS_D_V 512
 #define DS_KV_ROW_BYTES_BF16 1152
 #define DS_KV_ROW_BYTES_FP8 656
+#define DS_INDEXER_HEAD_DIM 128
 
 /* Device-side error bits ORed into *err_flag (when err_flag != NULL). */
 #define DS_DEVERR_IDX 1      /* an idx entry other than -1 outside [0, lens[row]) */
@@ -279,6 +280,48 @@ int ds_sparse_mla_decode_swa(const void* q, const void* kv_pages, int kv_dtype, 
 
 /* Workspace bytes of ds_sparse_mla_decode_swa (0 for an unsupported shape). */
 size_t ds_sparse_mla_swa_workspace_size(int64_t num_rows, int num_heads, int k, int swa_width);
+
+/*
+ * Indexer scores (the "MQA logits" that the top-k selects from). "[SM120]
+ * Sync DS4 with upstream main + validated perf backports" routes these
+ * logits through their own kernel and sizes a paged-MQA warm-up; "[Bugfix]
+ * Make DSV4 sparse MLA work end-to-end ...", section "What is fixed", gives
+ * the indexer one signed context length per query token. The pages give no
+ * formula; this library computes the lightning indexer of the
+ * DeepSeek-V3.2-Exp technical report: for query row r and position s,
+ *
+ *   logits[r, s] = sum_j weights[r, j] * max(0, q[r, j, :] . k[s, :])
+ *
+ * (multi-head queries, one shared key per position), with fp32 accumulation
+ * and the heads summed in order j = 0, 1, ...
+ *
+ *  q              bfloat16 [num_rows, num_heads, 128], 16-byte aligned.
+ *  weights        float32 [num_rows, num_heads].
+ *  k_pages        bfloat16 [num_pages, 64, 128] key cache, 16-byte aligned;
+ *                 the key of position s of a row is
+ *                 k_pages[block_table[req, s / 64], s % 64].
+ *  block_table    int32 [num_requests, bt_stride]; req = row_req[r], or r
+ *                 when row_req is NULL (then num_requests >= num_rows).
+ *  lens           int32 [num_rows]: row r scores positions 0 .. L_r - 1 with
+ *                 L_r = clamp(lens[r], 0, 64 * bt_stride), computed signed.
+ *  logits         float32 [num_rows, logits_stride], logits_stride >=
+ *                 64 * bt_stride; positions at or beyond L_r are not written.
+ *                 Feed it to ds_topk_per_row with row_starts = 0 and
+ *                 row_ends = lens (the same clamp applies there).
+ *  err_flag       optional int32 device word: DS_DEVERR_PAGE for a page id
+ *                 outside [0, num_pages) (its 64 positions score -inf),
+ *                 DS_DEVERR_ROWREQ for a row_req outside [0, num_requests)
+ *                 (the row scores nothing).
+ *
+ * Supported: num_heads 16, 32 or 64; head dim 128. A row's scores depend on
+ * that row's q, weights and keys alone (bitwise the same in any batch).
+ * Asynchronous on `stream`; allocates nothing.
+ */
+int ds_indexer_logits(const void* q, const float* weights, const void* k_pages,
+                      int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                      int64_t num_requests, const int32_t* row_req, const int32_t* lens,
+                      int64_t num_rows, int num_heads, int head_dim, float* logits,
+                      int64_t logits_stride, int32_t* err_flag, void* stream);
 
 /*
  * KV cache write: new latent rows into the paged cache, as bf16 rows or

@@ -14,6 +14,7 @@ from ._native import (  # noqa: F401
     DEVERR_TIMEOUT,
     EXPORTED,
     attention_workspace_size,
+    indexer_logits,
     kv_cache_write,
     last_error,
     lib,

@@ -75,6 +75,9 @@ def lib():
         L.ds_sparse_mla_swa_workspace_size.argtypes = [i64, i32, i32, i32]
         L.ds_kv_cache_write.restype = i32
         L.ds_kv_cache_write.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
+        L.ds_indexer_logits.restype = i32
+        L.ds_indexer_logits.argtypes = [vp, vp, vp, i64, vp, i64, i64, vp, vp, i64, i32, i32, vp,
+                                        i64, vp, vp]
         _lib = L
         return _lib
 
@@ -82,7 +85,7 @@ def lib():
 EXPORTED = ("ds_last_error", "ds_supported_config", "ds_topk_workspace_size",
             "ds_sparse_mla_workspace_size", "ds_topk_per_row", "ds_sparse_mla_decode",
             "ds_sparse_mla_prefill", "ds_sparse_mla_decode_noalloc", "ds_kv_cache_write",
-            "ds_sparse_mla_decode_swa", "ds_sparse_mla_swa_workspace_size")
+            "ds_sparse_mla_decode_swa", "ds_sparse_mla_swa_workspace_size", "ds_indexer_logits")
 
 
 def last_error():
@@ -286,3 +289,40 @@ def sparse_mla_decode_swa(q, kv_pages, kv_dtype, block_table, idx, lens, scale, 
         _ptr(swa_lens), W, _ptr(attn_sink), R, H, float(scale), _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream, dev)))
     return out, lse
+
+
+def indexer_logits(q, weights, k_pages, block_table, lens, row_req=None, logits=None,
+                   err_flag=None, stream=None):
+    """Indexer scores of every row: float32 [num_rows, 64 * bt_stride] (or
+    the given ``logits``); positions at or beyond a row's length are not
+    written. See ds_indexer_logits."""
+    _need(q, "q", torch.bfloat16, ndim=3)
+    dev = q.device
+    R, H, D = q.shape
+    _need(weights, "weights", torch.float32, dev, 2)
+    _need(k_pages, "k_pages", torch.bfloat16, dev, 3)
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(lens, "lens", torch.int32, dev, 1)
+    if tuple(weights.shape) != (R, H):
+        raise ValueError(f"weights must be [{R}, {H}], got {tuple(weights.shape)}")
+    if lens.numel() != R:
+        raise ValueError("lens must have one entry per row")
+    if k_pages.shape[1] != 64 or k_pages.shape[2] != D:
+        raise ValueError(f"k_pages must be [num_pages, 64, {D}], got {tuple(k_pages.shape)}")
+    if row_req is not None:
+        _need(row_req, "row_req", torch.int32, dev, 1)
+        if row_req.numel() != R:
+            raise ValueError("row_req must have one entry per row")
+    bt_stride = block_table.shape[1]
+    if logits is None:
+        logits = torch.empty((R, 64 * bt_stride), dtype=torch.float32, device=dev)
+    _need(logits, "logits", torch.float32, dev, 2)
+    if logits.shape[0] != R:
+        raise ValueError("logits must have one row per query row")
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32, dev, 1)
+    _check(lib().ds_indexer_logits(_ptr(q), _ptr(weights), _ptr(k_pages), k_pages.shape[0],
+                                   _ptr(block_table), bt_stride, block_table.shape[0],
+                                   _ptr(row_req), _ptr(lens), R, H, D, _ptr(logits),
+                                   logits.shape[1], _ptr(err_flag), _stream(stream, dev)))
+    return logits

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libds_sparse_mla.so"
-SOURCES = ["api.cu", "topk.cu", "attention.cu", "cache_write.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "topk.cu", "attention.cu", "cache_write.cu", "noalloc.cu", "indexer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

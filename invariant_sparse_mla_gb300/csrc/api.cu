@@ -307,6 +307,72 @@ int ds_kv_cache_write(const void* latent, int64_t num_rows, const int64_t* slots
   return ok();
 }
 
+int ds_indexer_logits(const void* q, const float* weights, const void* k_pages,
+                      int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                      int64_t num_requests, const int32_t* row_req, const int32_t* lens,
+                      int64_t num_rows, int num_heads, int head_dim, float* logits,
+                      int64_t logits_stride, int32_t* err_flag, void* stream) {
+  const char* fn = "ds_indexer_logits";
+  if (num_heads != 16 && num_heads != 32 && num_heads != 64)
+    return fail(DS_ERR_UNSUPPORTED, "%s: num_heads=%d is not supported; available: 16, 32, 64", fn,
+                num_heads);
+  if (head_dim != DS_INDEXER_HEAD_DIM)
+    return fail(DS_ERR_UNSUPPORTED, "%s: head_dim=%d is not supported; available: 128", fn,
+                head_dim);
+  if (num_rows < 0) return fail(DS_ERR_SHAPE, "%s: num_rows=%lld is negative", fn, (long long)num_rows);
+  if (num_pages < 1) return fail(DS_ERR_SHAPE, "%s: num_pages=%lld must be >= 1", fn, (long long)num_pages);
+  if (num_pages > (int64_t)INT32_MAX / DS_PAGE_BLOCK_SIZE)
+    return fail(DS_ERR_UNSUPPORTED, "%s: num_pages=%lld exceeds %lld (key rows are indexed in 32 bits)",
+                fn, (long long)num_pages, (long long)(INT32_MAX / DS_PAGE_BLOCK_SIZE));
+  if (bt_stride < 1) return fail(DS_ERR_SHAPE, "%s: bt_stride=%lld must be >= 1", fn, (long long)bt_stride);
+  if (bt_stride > (int64_t)INT32_MAX / DS_PAGE_BLOCK_SIZE)
+    return fail(DS_ERR_UNSUPPORTED, "%s: bt_stride=%lld is too large", fn, (long long)bt_stride);
+  if (num_requests < 1)
+    return fail(DS_ERR_SHAPE, "%s: num_requests=%lld must be >= 1", fn, (long long)num_requests);
+  if (logits_stride < DS_PAGE_BLOCK_SIZE * bt_stride)
+    return fail(DS_ERR_SHAPE,
+                "%s: logits_stride=%lld must be >= 64 * bt_stride = %lld (a row scores up to that "
+                "many positions)",
+                fn, (long long)logits_stride, (long long)(DS_PAGE_BLOCK_SIZE * bt_stride));
+  if (num_rows == 0) return ok();
+  if (num_rows > (int64_t)INT32_MAX / dsmla::indexer_chunks(bt_stride))
+    return fail(DS_ERR_UNSUPPORTED, "%s: num_rows=%lld is too large for one launch", fn,
+                (long long)num_rows);
+  struct {
+    const void* p;
+    const char* name;
+    uintptr_t align;
+  } ptrs[] = {{q, "q", 16},           {weights, "weights", 4}, {k_pages, "k_pages", 16},
+              {block_table, "block_table", 4}, {lens, "lens", 4}, {logits, "logits", 4}};
+  for (auto& x : ptrs) {
+    if (x.p == nullptr) return fail(DS_ERR_NULL, "%s: %s is NULL", fn, x.name);
+    if (!aligned(x.p, x.align))
+      return fail(DS_ERR_ALIGN, "%s: %s must be %d-byte aligned", fn, x.name, (int)x.align);
+  }
+  if (row_req != nullptr && !aligned(row_req, 4))
+    return fail(DS_ERR_ALIGN, "%s: row_req must be 4-byte aligned", fn);
+  if (err_flag != nullptr && !aligned(err_flag, 4))
+    return fail(DS_ERR_ALIGN, "%s: err_flag must be 4-byte aligned", fn);
+  dsmla::IndexerArgs a;
+  a.q = q;
+  a.w = weights;
+  a.k_pages = k_pages;
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.num_bt_rows = num_requests;
+  a.row_req = row_req;
+  a.lens = lens;
+  a.R = num_rows;
+  a.H = num_heads;
+  a.logits = logits;
+  a.logits_stride = logits_stride;
+  a.err_flag = err_flag;
+  cudaError_t e = dsmla::launch_indexer_logits(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
 size_t ds_sparse_mla_swa_workspace_size(int64_t num_rows, int num_heads, int k, int swa_width) {
   if (num_rows < 0) return 0;
   if (check_config("ds_sparse_mla_swa_workspace_size", num_heads, k, DS_PAGE_BLOCK_SIZE, DS_D_QK,

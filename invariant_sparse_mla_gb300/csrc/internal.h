@@ -75,6 +75,27 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
 
 cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream);
 
+// The indexer scores of ds_indexer_logits.
+struct IndexerArgs {
+  const void* q;              // bf16 [R, H, 128]
+  const float* w;             // [R, H]
+  const void* k_pages;        // bf16 [num_pages, 64, 128]
+  int64_t num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int64_t num_bt_rows;
+  const int32_t* row_req;     // nullptr: row r reads block-table row r
+  const int32_t* lens;        // [R]
+  int64_t R;
+  int H;
+  float* logits;              // [R, logits_stride]
+  int64_t logits_stride;
+  int32_t* err_flag;          // may be nullptr
+};
+
+cudaError_t launch_indexer_logits(const IndexerArgs& a, cudaStream_t stream);
+int64_t indexer_chunks(int64_t bt_stride);   // CTAs per row of one call
+
 cudaError_t launch_kv_cache_write(const void* latent, int64_t n, const int64_t* slots,
                                   int kv_dtype, void* pool, int64_t num_pages, int32_t* err,
                                   cudaStream_t stream);

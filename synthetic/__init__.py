@@ -242,6 +242,36 @@ def window_case(win_lens, W, kv_dtype="bf16", seed=7, device="cpu"):
     return pages, bt, idx.to(device), lens.to(device)
 
 
+@dataclass
+class IndexerCase:
+    """Indexer inputs: per-row queries and head weights, a paged key cache."""
+    name: str
+    q: torch.Tensor            # bfloat16 [R, H_I, 128]
+    w: torch.Tensor            # float32 [R, H_I]
+    k_pages: torch.Tensor      # bfloat16 [P, 64, 128]
+    block_table: torch.Tensor  # int32 [R, bt_stride]
+    lens: torch.Tensor         # int32 [R]
+    meta: dict = field(default_factory=dict)
+
+
+def indexer_case(name, ctx_lens, heads=64, dim=128, seed=8, device="cpu"):
+    """Indexer inputs for rows of the given context lengths: q and the keys
+    N(0,1) rounded to bf16, head weights N(0,1) / sqrt(heads) in float32, one
+    random permutation of the key pages handed to the rows in turn."""
+    ctx_lens = [int(c) for c in ctx_lens]
+    g = _gen(seed, device)
+    bt, num_pages = _block_table([max(1, c) for c in ctx_lens], g, device)
+    q = _normal((len(ctx_lens), heads, dim), g, device).to(torch.bfloat16)
+    w = _normal((len(ctx_lens), heads), g, device) / math.sqrt(heads)
+    k = torch.empty((num_pages, PAGE, dim), dtype=torch.bfloat16, device=device)
+    for p0 in range(0, num_pages, 4096):
+        p1 = min(num_pages, p0 + 4096)
+        k[p0:p1] = _normal(((p1 - p0), PAGE, dim), g, device).to(torch.bfloat16)
+    lens = torch.tensor(ctx_lens, dtype=torch.int32, device=device)
+    return IndexerCase(name=name, q=q, w=w, k_pages=k, block_table=bt, lens=lens,
+                       meta={"ctx_lens": ctx_lens, "seed": seed})
+
+
 def _uniform_ints(lo, hi, n, seed):
     g = torch.Generator().manual_seed(int(seed) + 1000003)
     return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
@@ -264,6 +294,19 @@ WORKLOADS = {
     "tp2_mtp4_decode": dict(kind="mtp", B=32, next_n=5, H=64, ctx=(4096, 32768), k=2048,
                             kv="bf16", scores="normal", seed=5, stride=32768),
 }
+
+
+# The indexer in front of the TP2-shaped decode batch: its rows' contexts,
+# 64 indexer heads of dimension 128 (the DeepSeek-V3.2 indexer's shape).
+INDEXER_WORKLOADS = {
+    "tp2_indexer": dict(B=32, ctx=(4096, 32768), ctx_seed=1, heads=64, dim=128, seed=8, k=2048),
+}
+
+
+def indexer_workload(name, device="cpu"):
+    w = INDEXER_WORKLOADS[name]
+    ctx = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["ctx_seed"])
+    return indexer_case(name, ctx, w["heads"], w["dim"], w["seed"], device)
 
 
 def workload_case(name, device="cpu", rows=None):

@@ -250,3 +250,28 @@ def test_split_geometry_fits_the_kernels(L):
             assert ws == S * R * H * 512 * 4 + 2 * ml, (k, W)
             T = (k + W) // 64
             assert S <= 4 and -(-T // S) <= 12, (k, W, S, T)
+
+
+def _ix(L, q=A, w=A, k=A, pages=16, bt=A, bts=8, nreq=4, row_req=None, lens=A, R=4, H=64, D=128,
+        logits=A, ls=512, err=None):
+    return L.ds_indexer_logits(q, w, k, pages, bt, bts, nreq, row_req, lens, R, H, D, logits, ls,
+                               err, None)
+
+
+@host_only
+def test_indexer_rejects_bad_arguments(L):
+    assert _ix(L, H=48) == DS_ERR_UNSUPPORTED and "num_heads=48" in _err(L)
+    assert _ix(L, D=64) == DS_ERR_UNSUPPORTED and "head_dim=64" in _err(L)
+    assert _ix(L, R=-1) == DS_ERR_SHAPE
+    assert _ix(L, pages=0) == DS_ERR_SHAPE and "num_pages" in _err(L)
+    assert _ix(L, bts=0) == DS_ERR_SHAPE and "bt_stride" in _err(L)
+    assert _ix(L, nreq=0) == DS_ERR_SHAPE and "num_requests" in _err(L)
+    # A row can score up to 64 * bt_stride positions: the output row must hold them.
+    assert _ix(L, ls=511) == DS_ERR_SHAPE and "logits_stride" in _err(L)
+    for name in ("q", "w", "k", "bt", "lens", "logits"):
+        assert _ix(L, **{name: None}) == DS_ERR_NULL, name
+    assert _ix(L, q=A + 8) == DS_ERR_ALIGN and "q must be 16-byte" in _err(L)
+    assert _ix(L, k=A + 4) == DS_ERR_ALIGN and "k_pages" in _err(L)
+    assert _ix(L, row_req=A + 2) == DS_ERR_ALIGN and "row_req" in _err(L)
+    # Zero rows is a valid empty call: nothing is launched.
+    assert _ix(L, R=0, q=None, w=None, k=None) in (DS_OK, DS_ERR_NULL)
