@@ -353,9 +353,12 @@ class Replayer:
     programmatic-launch overlap wherever a run starts); the rest replay one
     graph per set."""
 
+    MAX_RUN_GRAPH = 512   # a timed run of at most this many steps is one graph
+
     def __init__(self, stream, fn, sets):
         import torch
         self.stream = stream
+        self.sets = sets
 
         def capture(cases):
             g = torch.cuda.CUDAGraph()
@@ -364,6 +367,7 @@ class Replayer:
                     fn(c)
             return g
 
+        self.capture = capture
         n = len(sets)
         self.cycles = [capture(sets[k:] + sets[:k]) for k in range(n)]
         self.single = [capture([c]) for c in sets]
@@ -381,13 +385,24 @@ class Replayer:
                 self.pos = (self.pos + 1) % self.n
 
     def timed(self, steps):
-        """Seconds for `steps` steps, by CUDA events on the launching stream."""
+        """Seconds for `steps` steps, by CUDA events on the launching stream.
+        Up to MAX_RUN_GRAPH steps are captured (before the timed region) as
+        one graph of exactly those steps, so the region holds one launch."""
         import torch
+        run_graph = None
+        if steps <= self.MAX_RUN_GRAPH:
+            order = [self.sets[(self.pos + i) % self.n] for i in range(steps)]
+            run_graph = self.capture(order)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(self.stream)
-        self.run(steps)
+        if run_graph is not None:
+            with torch.cuda.stream(self.stream):
+                run_graph.replay()
+            self.pos = (self.pos + steps) % self.n
+        else:
+            self.run(steps)
         e1.record(self.stream)
         e1.synchronize()
         return e0.elapsed_time(e1) / 1e3
