@@ -95,8 +95,12 @@ def parse_args():
                     help="steps in flight in the end-to-end loop (each its own stream and buffers)")
     ap.add_argument("--sets", type=int, default=N_SETS,
                     help="rotating input sets (profiling runs use 1 to stay small)")
-    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESCS), default=WORKLOAD,
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESCS) + ["tp2_indexer"],
+                    default=WORKLOAD,
                     help="the TP2 decode batch is the headline; the others are for the record")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="keep only the first N rows of a decode or prefill workload (profiling "
+                         "captures of a reduced case)")
     args = ap.parse_args()
     if args.e2e_slots < 1:
         ap.error("--e2e-slots must be at least 1")
@@ -282,7 +286,7 @@ def job_value(world, rows_per_rank, steps, secs):
     return world * rows_per_rank * steps / secs
 
 
-def build_sets(wl, n_sets, rank, device):
+def build_sets(wl, n_sets, rank, device, rows=None):
     """`n_sets` independent input sets of workload `wl` (shifted seeds per
     set and rank; set 0 of rank 0 is the workload's own seed), each with its
     idx, out, lse and workspace buffers."""
@@ -296,6 +300,7 @@ def build_sets(wl, n_sets, rank, device):
         own = s == 0 and rank == 0
         if w["kind"] in ("decode", "decode_swa"):
             ctx = _uniform_ints(w["ctx"][0], w["ctx"][1], w["B"], w["seed"] if own else seed)
+            ctx = ctx[:rows] if rows else ctx
             c = decode_case(wl, ctx, w["H"], w["k"], w["kv"], w["seed"] if own else seed,
                             w["scores"], stride=w["stride"], device=device)
             if w["kind"] == "decode_swa":
@@ -308,7 +313,8 @@ def build_sets(wl, n_sets, rank, device):
             c = mtp_case(wl, lens, w["next_n"], w["H"], w["k"], w["kv"], w["seed"] if own else seed,
                          w["scores"], stride=w["stride"], device=device)
         else:
-            c = prefill_case(wl, w["ctx"], w["first_pos"], w["T"], w["H"], w["k"], w["kv"],
+            T = min(rows, w["T"]) if rows else w["T"]
+            c = prefill_case(wl, w["ctx"], w["first_pos"], T, w["H"], w["k"], w["kv"],
                              w["seed"] if own else seed, device=device)
         R, H, k = c.q.shape[0], c.H, c.k
         c.idx = torch.empty((R, k), dtype=torch.int32, device=device)
@@ -545,7 +551,7 @@ def run_ours(args, rank, world, local):
     wl = args.workload
     w = WORKLOADS[wl]
     n_sets = args.sets
-    sets = build_sets(wl, n_sets, rank, dev)
+    sets = build_sets(wl, n_sets, rank, dev, rows=args.rows)
     R, H, k = sets[0].q.shape[0], sets[0].H, sets[0].k
     stream = torch.cuda.Stream(device=dev)
     topk, decode, step = make_calls(ds, w["kind"], stream)
@@ -640,9 +646,11 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if args.rows:
+        line["config"]["rows_kept"] = args.rows
     if rank == 0 and not args.no_cpu_baseline and world == 1 and wl == WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(sets[0], budget_s=CPU_BASELINE_S)
-    if wl == WORKLOAD and not args.no_extra:
+    if wl == WORKLOAD and not args.no_extra and not args.rows:
         del rep_step, rep_topk, rep_dec, sets
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -965,6 +973,17 @@ def main():
         line = run_reference(args, rank, world)
     elif args.workload == "fp8_cache_write":
         line = run_cache_write(args, rank, world, local)
+    elif args.workload == "tp2_indexer":
+        import torch
+        import invariant_sparse_mla_gb300 as ds
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        res = measure_indexer(ds, dev, torch.cuda.Stream(device=dev), args.steps, args.warmup)
+        line = {"metric": METRIC + " [tp2_indexer]", "value": res["rows_per_s"] * world,
+                "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(res["step_us"] / 1e3, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded)", "config": {"workload": res["workload"]}, **res}
     else:
         line = run_ours(args, rank, world, local)
     if rank == 0 and line is not None:
