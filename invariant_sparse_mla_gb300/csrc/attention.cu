@@ -313,8 +313,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   constexpr int RW = RL::kRowsPerWarp, TG = RL::kTileGroups;
   constexpr int SWT = RL::kSoftmaxThreads;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base for the swizzled tiles, derived from the shared
+  // array by pointer arithmetic (not through an integer), so every access
+  // below stays a shared-memory access rather than a generic one.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kBars);
   uint32_t* vmask = reinterpret_cast<uint32_t*>(smem + LY::kMask);   // 2 words per tile

@@ -87,14 +87,6 @@ struct IxParams {
   int32_t* err;
 };
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx) {
-  asm volatile(
-      "{\n\t.reg .b64 st;\n\t"
-      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
-      "r"(tx)
-      : "memory");
-}
-
 // 64 rows x 64 bf16 of the key cache viewed as [num_pages * 64, 128]: rows
 // `y` .. y + 63, columns x .. x + 63, into 8 KB of 128-byte swizzled smem.
 __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -111,8 +103,9 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
                                                           const IxParams p) {
   using LY = IxLayout<NH>;
   extern __shared__ uint8_t ix_smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ix_smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base derived by pointer arithmetic on the shared
+  // array, so accesses through it stay shared-memory accesses.
+  uint8_t* smem = ix_smem_raw + ((1024u - (smem_u32(ix_smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kBars);
   float* w_s = reinterpret_cast<float*>(smem + LY::kW);

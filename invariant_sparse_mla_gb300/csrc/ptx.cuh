@@ -70,6 +70,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Arrives once on `bar` and adds `tx` bytes to the transfer count its
+// current phase waits for (the bytes asynchronous copies will deliver).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(tx)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global->shared copy through L2 only; src_bytes = 0 zero-fills.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
