@@ -136,7 +136,7 @@ struct Layout {
 // for a phase that cannot be overtaken by the next one, so the parity test
 // is unambiguous.
 enum Bar {
-  kQFull = 0,      // softmax threads' Q copies -> QK issuers (Q landed)
+  kQFull = 0,      // Q landed -> QK issuers (bf16: one expect-tx arrival; FP8: one per softmax thread)
   kKvFull = 1,     // 2: loader threads -> QK issuers (tile landed)
   kKvEmpty = 3,    // 2: PV issuer commit -> loaders (stage free), softmax (O^T holds the tile)
   kSFull = 5,      // 2: both QK issuers' commits -> softmax (S ready)
@@ -306,8 +306,12 @@ struct KParams {
   int32_t* err;
 };
 
+// `qmap` (bf16 pools only): q as a 2D tensor map [R * H rows, 576 bf16],
+// boxes of 64 columns x HG rows in the 128-byte swizzle (one box is one
+// K-major atom of the CTA's Q tile).
 template <int HG, bool FP8>
-__global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kernel(const KParams p) {
+__global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kernel(
+    const __grid_constant__ CUtensorMap qmap, const KParams p) {
   using LY = Layout<HG>;
   using RL = Roles<FP8>;
   constexpr int RW = RL::kRowsPerWarp, TG = RL::kTileGroups;
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
       // rest: one tcgen05.commit.
       uint32_t count = 1u;
       if (i == kPFull || i == kPFull + 1) count = (uint32_t)SWT;
-      if (i == kQFull) count = (uint32_t)SWT;
+      if (i == kQFull && FP8) count = (uint32_t)SWT;
       if (i >= kKvFull && i < kKvFull + kStages) count = RL::kLoaderThreads;
       if (i == kSFull || i == kSFull + 1) count = 2u;
       mbar_init(&bars[i], count);
@@ -410,10 +414,22 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   // entries, resolve pages and start the tile 0 and 1 copies; the softmax
   // warps copy Q.
   __syncthreads();   // barriers, TMEM and neff_s = 0 are visible before use
-  if (tid < SWT) {
-    // The softmax warps have nothing to do until the first S: they copy Q
-    // (requested into L2 before the wait) while the loaders look up entries,
-    // so Q's copies never queue ahead of a KV tile's.
+  if constexpr (!FP8) {
+    if (tid == 0) {
+      // Q by nine box copies (one per 64 columns), laid out by the copy
+      // engine in the swizzle the tensor cores read, through its own path:
+      // the loader warps' 16-byte copies of tiles 0 and 1 never queue behind
+      // Q's.
+      mbar_arrive_expect_tx(&bars[kQFull], (uint32_t)(HG * kRowBytesBf16));
+      const int y = (int)(row * p.H + (int64_t)hg * HG);
+#pragma unroll 1
+      for (int j = 0; j < kChunks / 8; ++j)
+        tma_load_box(sbase + LY::kQ + j * (HG * 128), &qmap, 64 * j, y, &bars[kQFull]);
+    }
+  } else if (tid < SWT) {
+    // FP8: the loaders fill tiles through registers, so nothing queues
+    // behind Q's 16-byte copies; the softmax warps, idle until the first S,
+    // copy it (measured faster here than the box copies).
     const __nv_bfloat16* qg = p.q + ((int64_t)row * p.H + (int64_t)hg * HG) * kD;
     for (int c = tid; c < HG * kChunks; c += SWT) {
       const int h = c / kChunks, ch = c - h * kChunks;
@@ -549,7 +565,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   bool failed = false;
   if (n_eff == 0) {
     // Nothing to attend to in this split: an empty partial.
-    if (producer || tid < SWT) cp_async_wait_all();  // copies land before the CTA exits
+    if (producer || (FP8 && tid < SWT)) cp_async_wait_all();  // copies land before the CTA exits
     if (tid < HG) {
       p.part_m[part_base + tid] = -INFINITY;
       p.part_l[part_base + tid] = 0.0f;
@@ -646,8 +662,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
           failed = true;
           break;
         }
-        // The tile (and Q) landed through cp.async, a generic-proxy write:
-        // order it before the tensor core's async-proxy reads.
+        // The tile (and, for FP8, Q) landed through generic-proxy writes:
+        // order them before the tensor core's async-proxy reads (bf16 Q came
+        // by the copy engine, itself an async-proxy write).
         fence_proxy_async_smem();
         tc_fence_after();
         const uint64_t b0 = kv_desc0 + (uint64_t)((sb * kStageBytes) >> 4);
@@ -836,7 +853,13 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     }
   }
 
-  if (tid < SWT) cp_async_wait_all();   // Q copies, on every path
+  // Q's copies land before the CTA exits, on every path (bf16: a bounded
+  // wait on the box copies).
+  if constexpr (FP8) {
+    if (tid < SWT) cp_async_wait_all();
+  } else {
+    if (tid == 0) (void)mbar_wait(&bars[kQFull], 0);
+  }
   if (failed && p.err != nullptr) atomicOr(p.err, kErrTimeout);
   tc_fence_before();
   const bool cta_failed = __syncthreads_or(failed);
@@ -918,8 +941,24 @@ cudaError_t launch_split(const KParams& kp, int64_t blocks, cudaStream_t stream)
   cudaError_t e = stream_device(stream, &dev);
   if (e == cudaSuccess) e = set_max_dynamic_smem(attr_once, dev, kern, LY::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // q viewed as [R * H rows, 576 columns] of bf16 (rows 1152 bytes apart);
+  // the FP8 kernel copies Q itself and never reads the map.
+  CUtensorMap qmap{};
+  if (FP8)
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(Roles<FP8>::kThreads), LY::kSmemBytes,
+                      stream, 1u, qmap, kp);
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)(kp.R * kp.H)};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kRowBytesBf16};
+  const cuuint32_t box[2] = {64, (cuuint32_t)HG};
+  const cuuint32_t estride[2] = {1, 1};
+  if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(kp.q), gdim,
+          gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   return launch_pdl(kern, dim3((unsigned)blocks), dim3(Roles<FP8>::kThreads), LY::kSmemBytes, stream,
-                    1u, kp);
+                    1u, qmap, kp);
 }
 
 }  // namespace

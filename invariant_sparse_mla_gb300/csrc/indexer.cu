@@ -87,17 +87,9 @@ struct IxParams {
   int32_t* err;
 };
 
-// 64 rows x 64 bf16 of the key cache viewed as [num_pages * 64, 128]: rows
-// `y` .. y + 63, columns x .. x + 63, into 8 KB of 128-byte swizzled smem.
-__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                             uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
+// The key cache is read as a 2D tensor map [num_pages * 64, 128] bf16: box
+// (0 or 64, page * 64) is 64 rows x 64 columns, 8 KB of 128-byte swizzled
+// shared memory.
 template <int NH>
 __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                           const IxParams p) {
@@ -286,31 +278,6 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, LY::kTmemCols);
-}
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static std::atomic<EncodeTiledFn> fn{nullptr};
-  EncodeTiledFn f = fn.load(std::memory_order_acquire);
-  if (f == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || ptr == nullptr) {
-      (void)cudaGetLastError();
-      return nullptr;
-    }
-    f = reinterpret_cast<EncodeTiledFn>(ptr);
-    fn.store(f, std::memory_order_release);
-  }
-  return f;
 }
 
 template <int NH>

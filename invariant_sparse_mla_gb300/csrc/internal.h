@@ -2,12 +2,38 @@
 #pragma once
 
 #include <stdint.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <utility>
 
 namespace dsmla {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); nullptr if the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || ptr == nullptr) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    f = reinterpret_cast<EncodeTiledFn>(ptr);
+    fn.store(f, std::memory_order_release);
+  }
+  return f;
+}
 
 // Entries per attention tile and tiles per split. The split count of a call
 // is ceil(k / kSplitEntries): a function of k alone, so a row's reduction

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <stdint.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace dsmla {
@@ -77,6 +78,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx
       "{\n\t.reg .b64 st;\n\t"
       "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
       "r"(tx)
+      : "memory");
+}
+
+// One box of a 2D tensor map (columns x.., rows y..) into shared memory at
+// `dst`, laid out as the map's swizzle mode says; completion adds the box's
+// bytes to `bar`'s transfer count. x times the element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                             uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
 
