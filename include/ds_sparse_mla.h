@@ -120,8 +120,9 @@ size_t ds_topk_workspace_size(int64_t num_rows, int64_t row_stride, int k);
 /*
  * Workspace bytes ds_sparse_mla_decode / ds_sparse_mla_prefill need for
  * num_rows query rows (decode requests or prefill tokens), num_heads heads
- * and top-k width k: the per-split partial results (float32). The number of
- * splits is a function of k alone. Returns 0 for an unsupported shape.
+ * and top-k width k: the per-split partial results (the unnormalised output
+ * rounded to bfloat16, the running maximum and sum in float32). The number
+ * of splits is a function of k alone. Returns 0 for an unsupported shape.
  */
 size_t ds_sparse_mla_workspace_size(int64_t num_rows, int num_heads, int k);
 

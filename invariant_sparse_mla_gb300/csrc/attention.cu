@@ -300,7 +300,7 @@ struct KParams {
   const int32_t* idx2;
   const int32_t* lens2;
   int k2;
-  float* part_o;
+  uint16_t* part_o;   // bf16 bits
   float* part_m;
   float* part_l;
   int32_t* err;
@@ -835,15 +835,17 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
     }
     if (!failed) {
       tc_fence_after();
-      // Epilogue: partial O (unnormalised, relative to m), m and l.
+      // Epilogue: partial O (unnormalised, relative to m) rounded to bf16,
+      // m and l in fp32.
       const int dv_lane = qd * 32 + lane;
-      float* po = p.part_o + part_base * kDv;
+      __nv_bfloat16* po = reinterpret_cast<__nv_bfloat16*>(p.part_o) + part_base * kDv;
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
         float v[HG];
         tmem_ld_cols<HG>(tmem + lane_base + kOCol + b * HG, v);
 #pragma unroll
-        for (int i = 0; i < HG; ++i) po[(int64_t)i * kDv + 128 * b + dv_lane] = v[i];
+        for (int i = 0; i < HG; ++i)
+          po[(int64_t)i * kDv + 128 * b + dv_lane] = __float2bfloat16_rn(v[i]);
       }
       const float lw = l + __shfl_xor_sync(0xffffffffu, l, 16);
       if (active && half == 0) {
@@ -876,7 +878,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 // Merges the splits of one (row, head) in split order (merge_weights,
 // merge_value), reading the partial results from the workspace. Every split's
 // m, l and O slice is loaded in one round before any arithmetic.
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ part_o,
                                                       const float* __restrict__ part_m,
                                                       const float* __restrict__ part_l,
                                                       int64_t R, int H, int S,
@@ -898,7 +900,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     if (s < S) {
       ms[s] = part_m[s * RH + rh];
       ls[s] = part_l[s * RH + rh];
-      os[s] = *reinterpret_cast<const float4*>(part_o + (s * RH + rh) * kDv + 4 * t);
+      const uint2 w = *reinterpret_cast<const uint2*>(part_o + (s * RH + rh) * kDv + 4 * t);
+      os[s] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                          __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
     }
   }
   const float sl = sink != nullptr ? sink[rh % H] * 1.4426950408889634f : -INFINITY;
@@ -966,7 +970,7 @@ cudaError_t launch_split(const KParams& kp, int64_t blocks, cudaStream_t stream)
 size_t attn_workspace_bytes(int64_t R, int H, int k, int k2) {
   const int64_t S = num_splits_total(k, k2);
   const int64_t n = S * R * H;
-  const size_t o = (size_t)n * kDv * sizeof(float);
+  const size_t o = (size_t)n * kDv * sizeof(uint16_t);
   const size_t ml = ((size_t)n * sizeof(float) + 255) & ~size_t(255);
   return o + 2 * ml;
 }
@@ -974,10 +978,10 @@ size_t attn_workspace_bytes(int64_t R, int H, int k, int k2) {
 AttnWorkspace attn_workspace_carve(void* base, int64_t R, int H, int k, int k2) {
   const int64_t S = num_splits_total(k, k2);
   const int64_t n = S * R * H;
-  const size_t o = (size_t)n * kDv * sizeof(float);
+  const size_t o = (size_t)n * kDv * sizeof(uint16_t);
   const size_t ml = ((size_t)n * sizeof(float) + 255) & ~size_t(255);
   AttnWorkspace w;
-  w.part_o = reinterpret_cast<float*>(base);
+  w.part_o = reinterpret_cast<uint16_t*>(base);
   w.part_m = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(base) + o);
   w.part_l = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(base) + o + ml);
   return w;
@@ -1025,7 +1029,7 @@ cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream) {
     e = fp8 ? launch_split<16, true>(kp, blocks, stream) : launch_split<16, false>(kp, blocks, stream);
   if (e != cudaSuccess) return e;
   return launch_pdl(combine_kernel, dim3((unsigned)(a.R * a.H)), dim3(128), 0, stream, 1u,
-                    (const float*)ws.part_o, (const float*)ws.part_m, (const float*)ws.part_l, a.R,
+                    (const uint16_t*)ws.part_o, (const float*)ws.part_m, (const float*)ws.part_l, a.R,
                     a.H, kp.num_splits, a.sink, reinterpret_cast<__nv_bfloat16*>(a.out), a.lse);
 }
 

@@ -88,7 +88,7 @@ struct AttnArgs {
 
 // Workspace layout of the attention path: partial O, m and l per split.
 struct AttnWorkspace {
-  float* part_o;  // [S, R, H, 512]
+  uint16_t* part_o;  // [S, R, H, 512] bf16 bits
   float* part_m;  // [S, R, H]  (log2 domain, scale folded in)
   float* part_l;  // [S, R, H]
 };

@@ -95,11 +95,12 @@ def test_supported_config_matrix(L):
 
 
 def test_workspace_sizes(L):
-    # splits = ceil(k / 512); per split: R*H*(512 + 2) floats, m/l 256-aligned.
+    # splits = ceil(k / 512); per split: R*H*512 bf16 partial O plus R*H floats
+    # each of m and l, 256-aligned.
     def want(R, H, k):
         n = -(-k // 512) * R * H
         ml = (n * 4 + 255) // 256 * 256
-        return n * 512 * 4 + 2 * ml
+        return n * 512 * 2 + 2 * ml   # bf16 partial O, fp32 m and l
     for R, H, k in [(1, 16, 64), (32, 64, 2048), (128, 128, 2048), (4096, 128, 2048), (3, 32, 576)]:
         if k % 64:
             assert L.ds_sparse_mla_workspace_size(R, H, k) == 0
@@ -238,8 +239,8 @@ def test_split_geometry_fits_the_kernels(L):
     # S = max(ceil(k / 512), ceil((k + W) / 768)). The split kernel holds at
     # most 12 tiles of 64 entries per split and the combine merges at most 4
     # splits, so every supported (k, W) must satisfy both. S is read back from
-    # the workspace size (S x R x H x (512 + 2) floats, the m and l arrays
-    # padded to 256 bytes).
+    # the workspace size (S x R x H x 512 bf16 partial values, then the fp32
+    # m and l arrays, each padded to 256 bytes).
     R, H = 1, 64
     for k in range(64, 2049, 64):
         for W in [0] + list(range(64, 513, 64)):
@@ -247,7 +248,7 @@ def test_split_geometry_fits_the_kernels(L):
             S = -(-k // 512)
             S = max(S, -(-(k + W) // 768))
             ml = -(-(S * R * H * 4) // 256) * 256
-            assert ws == S * R * H * 512 * 4 + 2 * ml, (k, W)
+            assert ws == S * R * H * 512 * 2 + 2 * ml, (k, W)
             T = (k + W) // 64
             assert S <= 4 and -(-T // S) <= 12, (k, W, S, T)
 
