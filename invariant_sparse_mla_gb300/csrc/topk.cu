@@ -823,7 +823,7 @@ struct StreamSmem {
   uint32_t cand_key[kStreamWarps * kStreamSeg];
   uint32_t sel[kStreamWords];   // selected positions
   uint32_t eqb[kStreamWords];   // positions tied with the threshold key
-  uint32_t hsmall[256];
+  uint32_t hsmall[3][256];      // one per refinement pass, zeroed with the row
   uint32_t scan_buf[32];
   uint32_t pick[3];
   uint32_t nseg[kStreamWarps];   // entries in each warp's segment
@@ -862,6 +862,53 @@ __device__ __forceinline__ void stream_pick(const uint32_t* hist, int nbins, uin
   take_in_bin = sm.pick[1];
   cnt = sm.pick[2];
   __syncthreads();
+}
+
+// One warp picks, among NBINS (16 or 256) bins counted in `hist`
+// (descending bin order), the bin holding the `take`-th largest key: lane l
+// sums bins NBINS-1-8l .. NBINS-8-8l, a warp scan finds the lane where the
+// count crosses `take`, and that lane walks its bins. Every warp that calls
+// it on the same counts gets the same (bin, count of that bin, take within
+// that bin), with no block barrier.
+template <int NBINS>
+__device__ __forceinline__ void warp_pick(const uint32_t* hist, uint32_t take, uint32_t& bin,
+                                          uint32_t& cnt, uint32_t& take_in_bin) {
+  constexpr int kPer = NBINS / 32 > 0 ? NBINS / 32 : 1;
+  const int lane = threadIdx.x & 31;
+  uint32_t c[kPer];
+  uint32_t mine = 0u;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int b = NBINS - 1 - (lane * kPer + q);
+    c[q] = b >= 0 ? hist[b] : 0u;
+    mine += c[q];
+  }
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t above = incl - mine;
+  // The crossing lane: the first whose inclusive count reaches take.
+  const uint32_t hit = __ballot_sync(0xffffffffu, incl >= take);
+  const int f = __ffs(hit) - 1;   // hit != 0: the bins sum to at least take
+  uint32_t rb = 0u, rc = 0u, rt = 0u;
+  if (lane == f) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int b = NBINS - 1 - (lane * kPer + q);
+      if (b >= 0 && above < take && take <= above + c[q]) {
+        rb = (uint32_t)b;
+        rc = c[q];
+        rt = take - above;
+      }
+      above += c[q];
+    }
+  }
+  bin = __shfl_sync(0xffffffffu, rb, f);
+  cnt = __shfl_sync(0xffffffffu, rc, f);
+  take_in_bin = __shfl_sync(0xffffffffu, rt, f);
 }
 
 // Clamped [start, end) of a row, as in every other kernel here: the length
@@ -1032,6 +1079,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
       sm.sel[i] = 0u;
       sm.eqb[i] = 0u;
     }
+    for (int i = tid; i < 3 * 256; i += kStreamThreads) (&sm.hsmall[0][0])[i] = 0u;
     if (tid == 0) sm.overflow = 0u;
     __syncthreads();
 
@@ -1067,27 +1115,29 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
       }
     }
 
-    // Resolve the low 20 bits among keys of bin P12: 8, 8, then 4 bits.
+    // Resolve the low 20 bits among keys of bin P12: 8, 8, then 4 bits,
+    // each pass with its own zeroed histogram and one block barrier (every
+    // warp picks for itself from the same counts).
     int shift = 20;
     for (int pass = 0; pass < 3 && cnt != take; ++pass) {
       const int width = pass < 2 ? 8 : 4;
       const int nshift = shift - width;
       const uint32_t dmask = (1u << width) - 1u;
-      if (tid < 256) sm.hsmall[tid] = 0u;
-      __syncthreads();
+      uint32_t* const hs = sm.hsmall[pass];
       if (list_ok) {
         for (uint32_t c = lane; c < nc; c += 32) {
           const uint32_t key = seg_key[c];
-          if ((key >> shift) == P) atomicAdd(&sm.hsmall[(key >> nshift) & dmask], 1u);
+          if ((key >> shift) == P) atomicAdd(&hs[(key >> nshift) & dmask], 1u);
         }
       } else {
         for (int i = tid; i < L; i += kStreamThreads) {
           const uint32_t key = score_key(p[i]);
-          if ((key >> shift) == P) atomicAdd(&sm.hsmall[(key >> nshift) & dmask], 1u);
+          if ((key >> shift) == P) atomicAdd(&hs[(key >> nshift) & dmask], 1u);
         }
       }
       __syncthreads();
-      stream_pick(sm.hsmall, 1 << width, take, sm, b, cnt, take);
+      if (width == 8) warp_pick<256>(hs, take, b, cnt, take);
+      else warp_pick<16>(hs, take, b, cnt, take);
       P = (P << width) | b;
       shift = nshift;
     }
