@@ -331,8 +331,16 @@ def build_sets(wl, n_sets, rank, device, rows=None):
 
 def make_calls(ds, kind, stream):
     """The public calls of one step: top-k, then the attention call."""
+    import torch
+    tk_ws = {}   # one top-k workspace per shape: the calls run in order on one stream
+
     def topk(c):
-        ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k, idx_out=c.idx, stream=stream)
+        shape = (c.scores.shape[0], c.scores.shape[1], c.k)
+        if shape not in tk_ws:
+            tk_ws[shape] = torch.empty(max(ds.topk_workspace_size(*shape), 1), dtype=torch.uint8,
+                                       device=c.scores.device)
+        ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k, idx_out=c.idx, stream=stream,
+                        workspace=tk_ws[shape])
 
     def decode(c):
         if kind == "decode":
@@ -707,6 +715,8 @@ def run_e2e(ds, sets, stream, dev, min_steps, min_secs, world, n_slots=E2E_SLOTS
         for n in in_names:
             hv[n].copy_(getattr(c, n).cpu())
         host_in.append(hb)
+    tk_bytes = max(max(ds.topk_workspace_size(c.scores.shape[0], c.scores.shape[1], c.k)
+                       for c in sets), 1)
     slots = []
     for _ in range(n_slots):
         din = torch.empty(max(b for b, _ in lay_in), dtype=torch.uint8, device=dev)
@@ -715,6 +725,7 @@ def run_e2e(ds, sets, stream, dev, min_steps, min_secs, world, n_slots=E2E_SLOTS
         slots.append({"din": din, "dinv": [views(din, sp) for _, sp in lay_in], "dout": dout,
                       "doutv": [views(dout, sp) for _, sp in lay_out], "hout": hout,
                       "ws": torch.empty_like(sets[0].ws),
+                      "tkws": torch.empty(tk_bytes, dtype=torch.uint8, device=dev),
                       "out_done": torch.cuda.Event(), "used": False})
     h2d = round(sum(b for b, _ in lay_in) / len(lay_in))     # bytes copied per step (mean)
     d2h = round(sum(b for b, _ in lay_out) / len(lay_out))
@@ -733,7 +744,7 @@ def run_e2e(ds, sets, stream, dev, min_steps, min_secs, world, n_slots=E2E_SLOTS
         st = torch.cuda.current_stream()
         sl["din"][:nin].copy_(hin, non_blocking=True)
         ds.topk_per_row(d["scores"], d["row_starts"], d["row_ends"], c.k, idx_out=o["idx"],
-                        stream=st)
+                        stream=st, workspace=sl["tkws"])
         ds.sparse_mla_decode(d["q"], c.kv_pages, c.kv_dtype, d["block_table"], o["idx"],
                              d["lens"], c.scale, out=o["out"], lse=o["lse"], workspace=sl["ws"],
                              stream=st)

@@ -24,4 +24,5 @@ from ._native import (  # noqa: F401
     supported_config,
     swa_workspace_size,
     topk_per_row,
+    topk_workspace_size,
 )

@@ -133,8 +133,18 @@ def attention_workspace_size(num_rows, num_heads, k):
     return int(lib().ds_sparse_mla_workspace_size(num_rows, num_heads, k))
 
 
-def topk_per_row(scores, row_starts, row_ends, k, idx_out=None, stream=None):
-    """Deterministic top-k of every row; returns int32 [num_rows, k]."""
+def topk_workspace_size(num_rows, row_stride, k):
+    return int(lib().ds_topk_workspace_size(num_rows, row_stride, k))
+
+
+def topk_per_row(scores, row_starts, row_ends, k, idx_out=None, stream=None, workspace=None):
+    """Deterministic top-k of every row; returns int32 [num_rows, k].
+
+    ``workspace``: None allocates the bytes ``topk_workspace_size`` asks for
+    (none for most shapes); a uint8 CUDA tensor is used as given; False runs
+    without one. The output is the same either way: the workspace only lets
+    the grid kernel run for the shapes that have it.
+    """
     _need(scores, "scores", torch.float32, ndim=2)
     dev = scores.device
     _need(row_starts, "row_starts", torch.int32, dev, 1)
@@ -147,8 +157,16 @@ def topk_per_row(scores, row_starts, row_ends, k, idx_out=None, stream=None):
     _need(idx_out, "idx_out", torch.int32, dev, 2)
     if tuple(idx_out.shape) != (R, k):
         raise ValueError(f"idx_out must be [{R}, {k}]")
+    if workspace is None:
+        need = topk_workspace_size(R, stride, k) if R > 0 else 0
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else False
+    if workspace is False:
+        ws_ptr, ws_bytes = None, 0
+    else:
+        _need(workspace, "workspace", torch.uint8, dev)
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel()
     _check(lib().ds_topk_per_row(_ptr(scores), stride, R, _ptr(row_starts), _ptr(row_ends), k,
-                                 _ptr(idx_out), None, 0, _stream(stream, dev)))
+                                 _ptr(idx_out), ws_ptr, ws_bytes, _stream(stream, dev)))
     return idx_out
 
 

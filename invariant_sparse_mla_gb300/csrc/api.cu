@@ -212,10 +212,10 @@ int ds_supported_config(int num_heads, int topk, int page_block_size, int d_qk, 
 }
 
 size_t ds_topk_workspace_size(int64_t num_rows, int64_t row_stride, int k) {
-  (void)num_rows;
-  (void)row_stride;
   (void)k;
-  return 0;
+  if (num_rows < 1 || num_rows > INT32_MAX || row_stride < 1 || row_stride > (int64_t(1) << 28))
+    return 0;
+  return dsmla::topk_workspace_bytes(num_rows, row_stride);
 }
 
 size_t ds_sparse_mla_workspace_size(int64_t num_rows, int num_heads, int k) {
@@ -229,8 +229,6 @@ size_t ds_sparse_mla_workspace_size(int64_t num_rows, int num_heads, int k) {
 int ds_topk_per_row(const float* scores, int64_t row_stride, int64_t num_rows,
                     const int32_t* row_starts, const int32_t* row_ends, int k, int32_t* idx_out,
                     void* workspace, size_t workspace_bytes, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   const char* fn = "ds_topk_per_row";
   if (k < 1 || k > 16384) return fail(DS_ERR_UNSUPPORTED, "%s: k=%d must be in [1, 16384]", fn, k);
   if (row_stride < 1 || row_stride > (int64_t(1) << 28))
@@ -247,7 +245,10 @@ int ds_topk_per_row(const float* scores, int64_t row_stride, int64_t num_rows,
   if (!aligned(scores, 4)) return fail(DS_ERR_ALIGN, "%s: scores must be 4-byte aligned", fn);
   if (!aligned(row_starts, 4) || !aligned(row_ends, 4) || !aligned(idx_out, 4))
     return fail(DS_ERR_ALIGN, "%s: row_starts, row_ends and idx_out must be 4-byte aligned", fn);
+  if (workspace != nullptr && !aligned(workspace, 256))
+    return fail(DS_ERR_ALIGN, "%s: workspace must be 256-byte aligned", fn);
   cudaError_t e = dsmla::launch_topk(scores, row_stride, num_rows, row_starts, row_ends, k, idx_out,
+                                     workspace, workspace_bytes,
                                      reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();

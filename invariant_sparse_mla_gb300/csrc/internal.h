@@ -96,8 +96,13 @@ struct AttnWorkspace {
 size_t attn_workspace_bytes(int64_t R, int H, int k, int k2 = 0);
 AttnWorkspace attn_workspace_carve(void* base, int64_t R, int H, int k, int k2 = 0);
 
+// Workspace bytes of the grid top-k for this shape (0: the shape takes a
+// kernel that needs none). With a workspace of at least this size the grid
+// kernel runs; without one, another kernel computes the same output.
+size_t topk_workspace_bytes(int64_t rows, int64_t stride);
 cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const int32_t* starts,
-                        const int32_t* ends, int k, int32_t* out, cudaStream_t stream);
+                        const int32_t* ends, int k, int32_t* out, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
 
 cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream);
 

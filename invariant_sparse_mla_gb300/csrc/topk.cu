@@ -8,17 +8,22 @@
 // the -1 padding follow "[Bugfix] Make DSV4 sparse MLA work end-to-end for
 // plain decode, MTP, and DSpark", section "What is fixed".
 //
-// Four kernels, chosen by the shape of the call alone:
+// Five kernels, chosen by the shape of the call (and, for the grid kernel,
+// by whether a workspace is given and the scores start 16-byte aligned):
 //   topk_smem_kernel     one CTA per row, the whole row in shared memory;
 //   topk_stream_kernel   a persistent grid, each CTA streaming whole rows;
+//   topk_grid_kernel     every row spread over the whole GPU: one cooperative
+//                        launch whose phases are separated by two grid
+//                        barriers (bounded waits on a workspace counter);
 //   topk_cluster_kernel  one thread-block cluster of up to 8 CTAs per row,
 //                        which exchange histograms and counts through
 //                        distributed shared memory between hardware cluster
 //                        barriers;
 //   topk_rows_kernel     one CTA per row, histogram passes over global memory.
-// No kernel spins on a flag written by another CTA. The selected set is
-// unique (the order is total), so every kernel gives the same bit-exact
-// output, and a row's output never depends on the rest of the batch.
+// Only the grid kernel waits on a value written by another CTA, and it is
+// launched cooperatively (every CTA resident). The selected set is unique
+// (the order is total), so every kernel gives the same bit-exact output, and
+// a row's output never depends on the rest of the batch.
 //
 // Key: the float's bits mapped to an unsigned integer whose order is the
 // float order (sign flipped for non-negatives, all bits flipped for
@@ -39,6 +44,7 @@
 #include <atomic>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dsmla {
 
@@ -1203,10 +1209,681 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Grid variant, for up to 256 rows of up to 131072 scores (8192 to 2^24
+// scores in all): every row is spread over the whole GPU. One cooperative
+// launch of one 1024-thread CTA per SM, all resident at once, runs three
+// phases separated by two grid barriers (a counter in the workspace, waited
+// on with a bounded spin):
+//   1. The score matrix (16-byte aligned) is viewed as rows of 256 scores;
+//      each row of the batch is cut into 8192-score segments starting at
+//      the view row that holds its first score, and the segments are dealt
+//      to the CTAs in contiguous runs. A CTA streams its run through a
+//      5-stage shared-memory ring, one tensor-map box (32 view rows, 32 KiB)
+//      per segment issued by one thread and completing on the stage's
+//      mbarrier, counts the 12-bit prefixes in shared memory and adds the
+//      counts of each row it touched to that row's histogram in the
+//      workspace (zeroed before the launch).
+//   2. Streaming its run again (from L2; the first copies are issued before
+//      the barrier), a CTA finds, for each row it touches, the threshold
+//      prefix T (the prefix of the row's k-th largest key) from the row's
+//      histogram, and lists every key whose prefix is at least T with its
+//      position: warps reserve slots in a shared-memory staging list, which
+//      goes to the row's list in the workspace with one global atomic add
+//      per row (a warp whose entries do not fit writes them there itself).
+//      The list's order is arbitrary.
+//   3. One CTA per row resolves the low 20 bits of the threshold on the
+//      list's prefix-T entries (8/8/4-bit histograms, as in the other
+//      kernels), marks the selected positions in a shared-memory bitmap,
+//      settles ties at the full key in a second bitmap (the lowest positions
+//      win, by one block scan) and writes the positions in ascending order
+//      (staged in shared memory, then stored contiguously).
+// The result is the same set as every other kernel's: the list's order only
+// changes which thread marks which bit.
+
+constexpr int kGrThreads = 1024;
+constexpr int kGrPer = 8;                    // scores per thread per segment (two 16-byte groups)
+constexpr int kGrSeg = kGrThreads * kGrPer;  // 8192 scores per segment
+constexpr int kGrStages = 5;                 // ring stages (segments in flight)
+constexpr int kGrView = 256;                 // scores per row of the 2D view
+constexpr int kGrBins = 4096;
+constexpr int kGrMaxRows = 256;
+constexpr int64_t kGrMaxStride = 131072;
+constexpr int64_t kGrMinScores = kGrSeg;
+constexpr int64_t kGrMaxScores = int64_t(1) << 24;
+constexpr int kGrWords = (int)(kGrMaxStride / 32);        // bitmap words of a row
+constexpr int kGrWordsPerThread = kGrWords / kGrThreads;  // 4
+constexpr int kGrTileQ = 8;                                // list entries per thread per tile
+constexpr int kGrTile = kGrThreads * kGrTileQ;
+constexpr int kGrStageCap = 4096;                          // staged list entries of one row
+constexpr int kGrOutStage = 8192;                          // output slots staged in shared memory
+constexpr uint32_t kGrNoPos = 0xFFFFFFFFu;
+constexpr long long kGrSpinCycles = 1ll << 31;   // about one second at the top SM clock
+constexpr size_t kGrRingBytes = (size_t)kGrStages * kGrSeg * sizeof(float);   // dynamic, 160 KiB
+static_assert(kGrRingBytes >= (2 * kGrWords + kGrOutStage) * sizeof(uint32_t),
+              "the bitmaps and the staged output alias the ring");
+
+// Workspace: a 256-byte header (the two barrier counters, then the error
+// word), the row histograms, the list lengths (these three zeroed before each
+// launch), the per-row threshold (prefix T, number of prefix-T keys taken),
+// then the lists, `stride` entries of (key, position) per row.
+constexpr size_t kGrHeader = 256;
+__host__ __device__ constexpr size_t gr_align(size_t b) { return (b + 255) & ~size_t(255); }
+__host__ __device__ constexpr size_t gr_hist_off() { return kGrHeader; }
+__host__ __device__ constexpr size_t gr_cnt_off(int64_t R) {
+  return gr_hist_off() + (size_t)R * kGrBins * sizeof(uint32_t);
+}
+__host__ __device__ constexpr size_t gr_zero_bytes(int64_t R) {
+  return gr_cnt_off(R) + gr_align((size_t)R * sizeof(uint32_t));
+}
+__host__ __device__ constexpr size_t gr_info_off(int64_t R) { return gr_zero_bytes(R); }
+__host__ __device__ constexpr size_t gr_list_off(int64_t R) {
+  return gr_info_off(R) + gr_align((size_t)R * sizeof(uint2));
+}
+
+struct GridArgs {
+  const float* scores;
+  int64_t stride;
+  int32_t rows;
+  int32_t k;
+  const int32_t* starts;
+  const int32_t* ends;
+  int32_t* out;
+  uint32_t* hdr;    // [0], [1]: barrier counters; [2]: error word
+  uint32_t* hist;   // [rows][4096]
+  uint32_t* cnt;    // [rows]: list lengths
+  uint2* info;      // [rows]: (T, keys of prefix T to take)
+  uint2* list;      // [rows][stride]: (key, position)
+};
+
+struct GridSmem {
+  uint32_t seg_off[kGrMaxRows + 1];   // segments before row r; rows with L <= k have none
+  int32_t len[kGrMaxRows];
+  int32_t g0[kGrMaxRows];             // score element of the row's position 0
+  union {
+    uint32_t hist[kGrBins];        // phase 1: one row's prefix counts
+    uint2 staged[kGrStageCap];     // phase 2: list entries of one row
+  } u;
+  uint32_t h[3][256];   // refinement histograms, one per pass
+  uint32_t wsum[32];
+  uint32_t pick[2];
+  uint32_t fill;        // staged slots reserved
+  uint32_t fit_end;     // first reservation that did not fit (~0: none)
+  uint32_t nflush, gbase;
+  alignas(8) uint64_t full[kGrStages];   // ring stage landed (transfer count)
+};
+
+// Every CTA arrives once; thread 0 waits until all `target` CTAs have, for at
+// most kGrSpinCycles, after which it sets the error word and goes on (the
+// cooperative launch makes every CTA resident, so the wait always ends).
+__device__ __forceinline__ void grid_barrier(uint32_t* counter, uint32_t target, uint32_t* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(counter, 1u);
+    const long long t0 = clock64();
+    for (;;) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+      if (v >= target) break;
+      if (clock64() - t0 > kGrSpinCycles) {
+        atomicOr(err, 1u);
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// The row holding segment `seg`: the last r with off[r] <= seg (off[0] = 0,
+// off[R] > seg), which is never an empty row.
+__device__ __forceinline__ int gr_row_of(const uint32_t* off, int R, uint32_t seg) {
+  int lo = 0, hi = R;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= seg) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Where a segment lies: row r, segment j of the row, the segment's first
+// score element A (a multiple of 256) and the row's elements [g0, gend).
+// Thread t's scores of the segment are elements A + 4t + 4096 h + i
+// (h = 0, 1; i = 0..3), at the same offsets in the ring stage.
+struct GrSeg {
+  int r;
+  uint32_t j;
+  int32_t A, g0, gend;
+};
+
+__device__ __forceinline__ void gr_locate(const GridSmem& sm, const GridArgs& a, uint32_t seg,
+                                          GrSeg& c) {
+  if (c.r < 0 || seg >= sm.seg_off[c.r + 1]) {
+    c.r = gr_row_of(sm.seg_off, a.rows, seg);
+    c.g0 = sm.g0[c.r];
+    c.gend = c.g0 + sm.len[c.r];
+  }
+  c.j = seg - sm.seg_off[c.r];
+  c.A = (c.g0 & ~(kGrView - 1)) + (int32_t)c.j * kGrSeg;
+}
+
+// One bit per in-row score of this thread (bit 4h + i).
+__device__ __forceinline__ uint32_t gr_valid(const GrSeg& c, int tid) {
+  if (c.A >= c.g0 && c.A + kGrSeg <= c.gend) return 0xFFu;   // an interior segment
+  uint32_t v = 0u;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int32_t e = c.A + 4 * tid + 4096 * h + i;
+      if (e >= c.g0 && e < c.gend) v |= 1u << (4 * h + i);
+    }
+  return v;
+}
+
+// Issues the copy of segment `c` into ring stage `st` (one thread): one box
+// of 32 view rows. View rows past the map (the matrix's last partial view
+// row and beyond) arrive as zeros.
+__device__ __forceinline__ void gr_issue(const CUtensorMap* smap, GridSmem& sm, float* ring,
+                                         const GrSeg& c, int st) {
+  uint64_t* const bar = &sm.full[st];
+  mbar_arrive_expect_tx(bar, kGrSeg * (uint32_t)sizeof(float));
+  tma_load_box(smem_u32(ring + st * kGrSeg), smap, 0, c.A / kGrView, bar);
+}
+
+// This thread's eight scores of the segment from its ring stage. Scores in
+// the matrix's last partial view row (elements from ncov on), which the map
+// does not cover, are read from global memory.
+__device__ __forceinline__ void gr_scores(const float* ring_stage, const GrSeg& c, int tid,
+                                          uint32_t valid, int32_t ncov,
+                                          const float* __restrict__ sc, float (&x)[kGrPer]) {
+  const float4 v0 = *reinterpret_cast<const float4*>(ring_stage + 4 * tid);
+  const float4 v1 = *reinterpret_cast<const float4*>(ring_stage + 4096 + 4 * tid);
+  x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+  x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+  if (c.A + kGrSeg > ncov) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int32_t e = c.A + 4 * tid + 4096 * h + i;
+        if (((valid >> (4 * h + i)) & 1u) && e >= ncov) x[4 * h + i] = sc[e];
+      }
+  }
+}
+
+// Adds the shared-memory counts of row r to its histogram in the workspace
+// and clears them.
+__device__ __forceinline__ void gr_flush_hist(const GridArgs& a, GridSmem& sm, int r) {
+  __syncthreads();
+  uint32_t* const gh = a.hist + (size_t)r * kGrBins;
+  for (int i = threadIdx.x; i < kGrBins; i += kGrThreads) {
+    const uint32_t c = sm.u.hist[i];
+    if (c) atomicAdd(gh + i, c);
+    sm.u.hist[i] = 0u;
+  }
+  __syncthreads();
+}
+
+// Moves the staged entries of row r to its list in the workspace.
+__device__ __forceinline__ void gr_flush_list(const GridArgs& a, GridSmem& sm, int r) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t v = sm.fill < sm.fit_end ? sm.fill : sm.fit_end;
+    sm.nflush = v;
+    sm.gbase = v ? atomicAdd(a.cnt + r, v) : 0u;
+    sm.fill = 0u;
+    sm.fit_end = ~0u;
+  }
+  __syncthreads();
+  const uint32_t v = sm.nflush, gb = sm.gbase;
+  uint2* const lr = a.list + (int64_t)r * a.stride + gb;
+  for (uint32_t i = threadIdx.x; i < v; i += kGrThreads) lr[i] = sm.u.staged[i];
+  __syncthreads();
+}
+
+// Threshold prefix of row r from its histogram: sm.pick = (T, number of keys
+// whose prefix is above T). Thread t reads bins 4095 - 4t - q, q = 0..3.
+constexpr int kGrBinsPerThread = kGrBins / kGrThreads;
+static_assert(kGrBinsPerThread == 4, "one 16-byte load of bins per thread");
+__device__ __forceinline__ void gr_threshold(const GridArgs& a, GridSmem& sm, int r) {
+  const int tid = threadIdx.x;
+  const uint32_t k = (uint32_t)a.k;
+  const uint32_t* gh = a.hist + (size_t)r * kGrBins;
+  const uint4 b4 = __ldcg(reinterpret_cast<const uint4*>(gh + kGrBins - 4 - 4 * tid));
+  const uint32_t c[4] = {b4.w, b4.z, b4.y, b4.x};
+  const uint32_t mine = c[0] + c[1] + c[2] + c[3];
+  uint32_t tot;
+  uint32_t above = block_exclusive_scan_nt<kGrThreads>(mine, sm.wsum, tot);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (above < k && k <= above + c[q]) {
+      sm.pick[0] = (uint32_t)(kGrBins - 1 - 4 * tid - q);
+      sm.pick[1] = above;
+    }
+    above += c[q];
+  }
+  __syncthreads();
+}
+
+// Phase 3 for row r. On entry the bitmaps and refinement histograms are
+// zero; they are zero again on return.
+__device__ __forceinline__ void grid_resolve(const GridArgs& a, GridSmem& sm, uint32_t* sel,
+                                             uint32_t* tie, int32_t* out_s, int r) {
+  const int tid = threadIdx.x;
+  const int L = sm.len[r];
+  const uint32_t k = (uint32_t)a.k;
+  int32_t* __restrict__ orow = a.out + (int64_t)r * a.k;
+  if (L <= a.k) {
+    for (int j = tid; j < a.k; j += kGrThreads) orow[j] = j < L ? j : -1;
+    return;
+  }
+  const uint2* __restrict__ lr = a.list + (int64_t)r * a.stride;
+  // The first tile is read together with the list length (from the part of
+  // the row's list that exists), then trimmed to it.
+  const uint32_t cap = a.stride < kGrTile ? (uint32_t)a.stride : (uint32_t)kGrTile;
+  uint2 e[kGrTileQ];
+#pragma unroll
+  for (int q = 0; q < kGrTileQ; ++q) {
+    const uint32_t i = (uint32_t)(q * kGrThreads + tid);
+    e[q] = i < cap ? __ldcg(lr + i) : make_uint2(0u, kGrNoPos);
+  }
+  const uint2 inf = __ldcg(a.info + r);
+  uint32_t n = __ldcg(a.cnt + r);
+  if (n > (uint32_t)L) {   // only after a barrier gave up
+    atomicOr(a.hdr + 2, 2u);
+    n = (uint32_t)L;
+  }
+  auto trim = [&](uint32_t t) {
+#pragma unroll
+    for (int q = 0; q < kGrTileQ; ++q) {
+      const uint32_t i = t * kGrTile + (uint32_t)(q * kGrThreads + tid);
+      if (i >= n || e[q].y >= (uint32_t)L) e[q].y = kGrNoPos;
+    }
+  };
+  auto load_tile = [&](uint32_t t) {
+#pragma unroll
+    for (int q = 0; q < kGrTileQ; ++q) {
+      const uint32_t i = t * kGrTile + (uint32_t)(q * kGrThreads + tid);
+      e[q] = i < n ? __ldcg(lr + i) : make_uint2(0u, kGrNoPos);
+    }
+    trim(t);
+  };
+  const uint32_t ntiles = (n + kGrTile - 1) / kGrTile;
+  trim(0);
+
+  // Threshold state as in the other kernels: prefix P at `shift` dropped
+  // bits; `take` of the `cnt` keys with that prefix are selected.
+  uint32_t P = inf.x, take = inf.y, cnt = n - (k - inf.y);
+  int shift = 20;
+  for (int pass = 0; pass < 3 && cnt != take; ++pass) {
+    const int width = pass < 2 ? 8 : 4;
+    const int nshift = shift - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    uint32_t* const hs = sm.h[pass];
+    for (uint32_t t = 0; t < ntiles; ++t) {
+      if (ntiles > 1) load_tile(t);
+#pragma unroll
+      for (int q = 0; q < kGrTileQ; ++q)
+        if (e[q].y != kGrNoPos && (e[q].x >> shift) == P)
+          atomicAdd(&hs[(e[q].x >> nshift) & dmask], 1u);
+    }
+    __syncthreads();
+    uint32_t b;
+    if (width == 8) warp_pick<256>(hs, take, b, cnt, take);
+    else warp_pick<16>(hs, take, b, cnt, take);
+    P = (P << width) | b;
+    shift = nshift;
+  }
+  const bool all_eq = cnt == take;
+  for (uint32_t t = 0; t < ntiles; ++t) {
+    if (ntiles > 1) load_tile(t);
+#pragma unroll
+    for (int q = 0; q < kGrTileQ; ++q) {
+      if (e[q].y == kGrNoPos) continue;
+      const uint32_t hi = e[q].x >> shift;
+      const uint32_t bit = 1u << (e[q].y & 31u);
+      if (hi > P || (hi == P && all_eq)) atomicOr(&sel[e[q].y >> 5], bit);
+      else if (hi == P) atomicOr(&tie[e[q].y >> 5], bit);
+    }
+  }
+  __syncthreads();
+
+  // Thread t owns bitmap words [4t, 4t + 4): positions [128t, 128t + 128).
+  const int nw = (L + 31) >> 5;
+  uint32_t w[kGrWordsPerThread];
+#pragma unroll
+  for (int i = 0; i < kGrWordsPerThread; ++i) {
+    const int wi = kGrWordsPerThread * tid + i;
+    w[i] = wi < nw ? sel[wi] : 0u;
+  }
+  if (!all_eq) {
+    uint32_t tw[kGrWordsPerThread], c = 0u;
+#pragma unroll
+    for (int i = 0; i < kGrWordsPerThread; ++i) {
+      const int wi = kGrWordsPerThread * tid + i;
+      tw[i] = wi < nw ? tie[wi] : 0u;
+      c += __popc(tw[i]);
+    }
+    uint32_t tot;
+    const uint32_t before = block_exclusive_scan_nt<kGrThreads>(c, sm.wsum, tot);
+    if (before < take) {
+      uint32_t rem = take - before;
+#pragma unroll
+      for (int i = 0; i < kGrWordsPerThread; ++i) {
+        const uint32_t m = first_set_bits(tw[i], rem);
+        w[i] |= m;
+        rem -= __popc(m);
+      }
+    }
+  }
+  uint32_t c = 0u;
+#pragma unroll
+  for (int i = 0; i < kGrWordsPerThread; ++i) c += __popc(w[i]);
+  uint32_t total;
+  uint32_t pos = block_exclusive_scan_nt<kGrThreads>(c, sm.wsum, total);
+  // Clear this thread's words and the histograms for the next row.
+#pragma unroll
+  for (int i = 0; i < kGrWordsPerThread; ++i) {
+    const int wi = kGrWordsPerThread * tid + i;
+    if (wi < nw) {
+      sel[wi] = 0u;
+      tie[wi] = 0u;
+    }
+  }
+  for (int i = tid; i < 3 * 256; i += kGrThreads) (&sm.h[0][0])[i] = 0u;
+  // Output slots below kGrOutStage go through shared memory, so that the
+  // stores to idx_out are contiguous; higher slots (k > 8192) go direct.
+#pragma unroll
+  for (int i = 0; i < kGrWordsPerThread; ++i) {
+    const int base = 32 * (kGrWordsPerThread * tid + i);
+    for (uint32_t m = w[i]; m; m &= m - 1u) {
+      const int v = base + __ffs(m) - 1;
+      if (pos < (uint32_t)kGrOutStage) out_s[pos] = v;
+      else if (pos < k) orow[pos] = v;
+      ++pos;
+    }
+  }
+  __syncthreads();
+  const int nout = a.k < kGrOutStage ? a.k : kGrOutStage;
+  for (int j = tid; j < nout; j += kGrThreads) orow[j] = out_s[j];
+}
+
+__global__ void __launch_bounds__(kGrThreads, 1)
+    topk_grid_kernel(const __grid_constant__ CUtensorMap smap, const GridArgs a) {
+  __shared__ GridSmem sm;
+  extern __shared__ __align__(128) float gr_ring[];   // [kGrStages][kGrSeg]
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int R = a.rows;
+  const uint32_t G = gridDim.x;
+  const uint32_t k = (uint32_t)a.k;
+
+  if (tid == 0) {
+    for (int s = 0; s < kGrStages; ++s) mbar_init(&sm.full[s], 1);
+    mbar_fence_init();
+    sm.fill = 0u;
+    sm.fit_end = ~0u;
+  }
+  // Row table: clamped length, start and segment offsets of every row.
+  uint32_t ns = 0u;
+  if (tid < R) {
+    const int64_t s = a.starts[tid];
+    const int64_t e = a.ends[tid];
+    int L = 0;
+    if (s >= 0 && s <= a.stride) {
+      int64_t L64 = e - s;
+      if (L64 < 0) L64 = 0;
+      if (L64 > a.stride - s) L64 = a.stride - s;
+      L = (int)L64;
+    }
+    const int32_t g0 = (int32_t)(tid * a.stride + (s >= 0 && s <= a.stride ? s : 0));
+    sm.len[tid] = L;
+    sm.g0[tid] = g0;
+    if (L > a.k) ns = (uint32_t)(((g0 & (kGrView - 1)) + L + kGrSeg - 1) / kGrSeg);
+  }
+  for (int i = tid; i < kGrBins; i += kGrThreads) sm.u.hist[i] = 0u;
+  uint32_t S;
+  const uint32_t ex = block_exclusive_scan_nt<kGrThreads>(ns, sm.wsum, S);
+  if (tid <= R) sm.seg_off[tid] = ex;   // thread R's exclusive sum is the total
+  __syncthreads();
+  const uint32_t sb = (uint32_t)((uint64_t)S * blockIdx.x / G);
+  const uint32_t se = (uint32_t)((uint64_t)S * (blockIdx.x + 1) / G);
+  const int32_t ncov = (int32_t)(((int64_t)R * a.stride) & ~int64_t(kGrView - 1));
+
+  // The ring: segment sb + i goes to stage i % kGrStages. Thread 0 fills the
+  // stages; every thread waits for a stage's copies, reads its 16 bytes, and
+  // after the block barrier that ends each segment thread 0 refills the
+  // stage with the segment kGrStages further on. `par` holds the parity of
+  // each stage's next phase.
+  GrSeg ic, pc;
+  uint32_t par = 0u;
+  bool late = false;   // a ring wait gave up
+  auto prime = [&]() {
+    if (tid == 0) {
+      ic.r = -1;
+      for (int s = 0; s < kGrStages && sb + s < se; ++s) {
+        gr_locate(sm, a, sb + s, ic);
+        gr_issue(&smap, sm, gr_ring, ic, s);
+      }
+    }
+  };
+  auto take_stage = [&](uint32_t seg, uint32_t valid, float (&x)[kGrPer]) {
+    const int st = (int)((seg - sb) % kGrStages);
+    if (!mbar_wait(&sm.full[st], (par >> st) & 1u)) late = true;
+    par ^= 1u << st;
+    gr_scores(gr_ring + st * kGrSeg, pc, tid, valid, ncov, a.scores, x);
+  };
+  auto release_stage = [&](uint32_t seg) {
+    __syncthreads();   // every thread has read the stage
+    const uint32_t nx = seg + kGrStages;
+    if (tid == 0 && nx < se) {
+      gr_locate(sm, a, nx, ic);
+      gr_issue(&smap, sm, gr_ring, ic, (int)((nx - sb) % kGrStages));
+    }
+  };
+
+  // Phase 1: 12-bit prefix counts.
+  prime();
+  pc.r = -1;
+  int cur = -1;
+  for (uint32_t seg = sb; seg < se; ++seg) {
+    gr_locate(sm, a, seg, pc);
+    if (pc.r != cur) {
+      if (cur >= 0) gr_flush_hist(a, sm, cur);
+      cur = pc.r;
+    }
+    const uint32_t valid = gr_valid(pc, tid);
+    float x[kGrPer];
+    take_stage(seg, valid, x);
+#pragma unroll
+    for (int q = 0; q < kGrPer; ++q)
+      if ((valid >> q) & 1u) atomicAdd(&sm.u.hist[score_key(x[q]) >> 20], 1u);
+    release_stage(seg);
+  }
+  if (cur >= 0) gr_flush_hist(a, sm, cur);
+
+  // The scores are read-only: phase 2's first copies go out before the wait.
+  prime();
+  grid_barrier(a.hdr, G, a.hdr + 2);
+
+  // Phase 2: threshold prefix of each row touched, then the lists.
+  pc.r = -1;
+  cur = -1;
+  uint32_t lo_key = 0u;   // a key's prefix is at least T iff key >= lo_key
+  for (uint32_t seg = sb; seg < se; ++seg) {
+    gr_locate(sm, a, seg, pc);
+    if (pc.r != cur) {
+      if (cur >= 0) gr_flush_list(a, sm, cur);
+      cur = pc.r;
+      gr_threshold(a, sm, cur);
+      const uint32_t T = sm.pick[0];
+      if (pc.j == 0 && tid == 0) a.info[cur] = make_uint2(T, k - sm.pick[1]);
+      lo_key = T << 20;
+    }
+    const uint32_t valid = gr_valid(pc, tid);
+    float x[kGrPer];
+    take_stage(seg, valid, x);
+    uint32_t kk[kGrPer];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int q = 0; q < kGrPer; ++q) {
+      kk[q] = score_key(x[q]);
+      if (((valid >> q) & 1u) && kk[q] >= lo_key) m |= 1u << q;
+    }
+    const uint32_t cm = __popc(m);
+    uint32_t incl = cm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t wt = __shfl_sync(0xffffffffu, incl, 31);
+    if (wt != 0u) {
+      uint32_t base = 0u;
+      if (lane == 31) base = atomicAdd(&sm.fill, wt);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      const uint32_t p0 = (uint32_t)(pc.A + 4 * tid - pc.g0);   // position of score q = 0
+      if (base + wt <= (uint32_t)kGrStageCap) {
+        uint32_t o = base + incl - cm;
+#pragma unroll
+        for (int q = 0; q < kGrPer; ++q)
+          if ((m >> q) & 1u)
+            sm.u.staged[o++] = make_uint2(kk[q], p0 + (uint32_t)(4096 * (q >> 2) + (q & 3)));
+      } else {
+        // Staging full: this warp's entries go to the row's list directly.
+        uint32_t gb = 0u;
+        if (lane == 31) {
+          atomicMin(&sm.fit_end, base);
+          gb = atomicAdd(a.cnt + cur, wt);
+        }
+        uint32_t o = __shfl_sync(0xffffffffu, gb, 31) + incl - cm;
+        uint2* const lr = a.list + (int64_t)cur * a.stride;
+#pragma unroll
+        for (int q = 0; q < kGrPer; ++q)
+          if ((m >> q) & 1u) lr[o++] = make_uint2(kk[q], p0 + (uint32_t)(4096 * (q >> 2) + (q & 3)));
+      }
+    }
+    release_stage(seg);
+  }
+  if (cur >= 0) gr_flush_list(a, sm, cur);
+  if (late && tid == 0) atomicOr(a.hdr + 2, 4u);
+
+  // Every copy issued has been waited for: the ring's space becomes the two
+  // bitmaps and the staged output of phase 3.
+  uint32_t* const sel = reinterpret_cast<uint32_t*>(gr_ring);
+  uint32_t* const tie = sel + kGrWords;
+  int32_t* const out_s = reinterpret_cast<int32_t*>(tie + kGrWords);
+  for (int i = tid; i < 2 * kGrWords; i += kGrThreads) sel[i] = 0u;
+  for (int i = tid; i < 3 * 256; i += kGrThreads) (&sm.h[0][0])[i] = 0u;
+  grid_barrier(a.hdr + 1, G, a.hdr + 2);
+  pdl_trigger();
+
+  // Phase 3: one CTA per row.
+  for (int r = blockIdx.x; r < R; r += (int)G) {
+    grid_resolve(a, sm, sel, tie, out_s, r);
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+bool topk_grid_shape(int64_t rows, int64_t stride) {
+  if (rows < 1 || rows > kGrMaxRows || stride > kGrMaxStride || rows * stride > kGrMaxScores ||
+      rows * stride < kGrMinScores)
+    return false;
+  if (stride <= kRowMaxLen && rows >= kRowMinRows) return false;      // whole rows in shared memory
+  if (stride <= kStreamMaxLen && rows >= kStreamMinRows) return false;  // the streaming grid
+  return true;
+}
+
+size_t topk_workspace_bytes(int64_t rows, int64_t stride) {
+  if (!topk_grid_shape(rows, stride)) return 0;
+  return gr_list_off(rows) + (size_t)rows * (size_t)stride * sizeof(uint2);
+}
+
+namespace {
+
+// CTAs of one grid top-k launch on device `dev`: every CTA resident at once.
+struct PerDeviceCount {
+  std::atomic<int> v[PerDeviceOnce::kMaxDevices] = {};
+};
+
+cudaError_t grid_ctas(int dev, int* ctas) {
+  static PerDeviceCount cache;
+  const bool tracked = dev >= 0 && dev < PerDeviceOnce::kMaxDevices;
+  if (tracked && (*ctas = cache.v[dev].load(std::memory_order_acquire)) > 0) return cudaSuccess;
+  int sms = 0, occ = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, topk_grid_kernel, kGrThreads,
+                                                    kGrRingBytes);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) return cudaErrorCooperativeLaunchTooLarge;
+  *ctas = sms * occ;
+  if (tracked) cache.v[dev].store(*ctas, std::memory_order_release);
+  return cudaSuccess;
+}
+
+cudaError_t launch_topk_grid(const float* scores, int64_t stride, int64_t rows,
+                             const int32_t* starts, const int32_t* ends, int k, int32_t* out,
+                             void* workspace, int dev, cudaStream_t stream) {
+  static PerDeviceOnce grid_attr;
+  cudaError_t e = set_max_dynamic_smem(grid_attr, dev, topk_grid_kernel, (int)kGrRingBytes);
+  if (e != cudaSuccess) return e;
+  int G = 0;
+  e = grid_ctas(dev, &G);
+  if (e != cudaSuccess) return e;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  e = cudaMemsetAsync(ws, 0, gr_zero_bytes(rows), stream);
+  if (e != cudaSuccess) return e;
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // The score matrix as whole rows of 256 scores (a partial last view row is
+  // left out of the map and read with plain loads).
+  CUtensorMap smap;
+  const cuuint64_t gdim[2] = {(cuuint64_t)kGrView, (cuuint64_t)(rows * stride / kGrView)};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kGrView * sizeof(float)};
+  const cuuint32_t box[2] = {(cuuint32_t)kGrView, (cuuint32_t)(kGrSeg / kGrView)};
+  const cuuint32_t estride[2] = {1, 1};
+  if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(scores), gdim, gstride, box,
+          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  GridArgs a;
+  a.scores = scores;
+  a.stride = stride;
+  a.rows = (int32_t)rows;
+  a.k = k;
+  a.starts = starts;
+  a.ends = ends;
+  a.out = out;
+  a.hdr = reinterpret_cast<uint32_t*>(ws);
+  a.hist = reinterpret_cast<uint32_t*>(ws + gr_hist_off());
+  a.cnt = reinterpret_cast<uint32_t*>(ws + gr_cnt_off(rows));
+  a.info = reinterpret_cast<uint2*>(ws + gr_info_off(rows));
+  a.list = reinterpret_cast<uint2*>(ws + gr_list_off(rows));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(kGrThreads);
+  cfg.dynamicSmemBytes = kGrRingBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_grid_kernel, smap, a);
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const int32_t* starts,
-                        const int32_t* ends, int k, int32_t* out, cudaStream_t stream) {
+                        const int32_t* ends, int k, int32_t* out, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   // The kernel depends on the shapes alone, and the selected set is unique,
   // so the choice never changes the output:
@@ -1219,6 +1896,12 @@ cudaError_t launch_topk(const float* scores, int64_t stride, int64_t rows, const
   int dev = 0;
   cudaError_t e = stream_device(stream, &dev);
   if (e != cudaSuccess) return e;
+  // The grid kernel reads the scores with tensor-map copies: their start must
+  // be 16-byte aligned (other pointers take the kernels below).
+  const size_t grid_ws = topk_workspace_bytes(rows, stride);
+  if (grid_ws != 0 && workspace != nullptr && workspace_bytes >= grid_ws &&
+      (reinterpret_cast<uintptr_t>(scores) & 15u) == 0u)
+    return launch_topk_grid(scores, stride, rows, starts, ends, k, out, workspace, dev, stream);
   if (stride <= kRowMaxLen && rows >= kRowMinRows) {
     static PerDeviceOnce row_attr;
     e = set_max_dynamic_smem(row_attr, dev, topk_smem_kernel, (int)sizeof(RowSmem));

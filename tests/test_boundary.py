@@ -110,8 +110,34 @@ def test_workspace_sizes(L):
     assert L.ds_topk_workspace_size(100, 1000, 10) == 0
 
 
+def test_topk_workspace_sizes(L):
+    # The grid top-k's workspace: a 256-byte header, a 4096-bin histogram and
+    # a list length per row (zeroed before each launch), the per-row
+    # threshold, then `stride` (key, position) entries per row; shapes taken
+    # by the other kernels need none.
+    def al(b):
+        return (b + 255) // 256 * 256
+
+    def want(R, stride):
+        return 256 + R * 4096 * 4 + al(R * 4) + al(R * 8) + R * stride * 8
+    for R, stride in [(128, 131072), (8, 100000), (1, 16384), (15, 32768), (255, 65536),
+                      (16, 70000), (1, 8192)]:
+        assert L.ds_topk_workspace_size(R, stride, 2048) == want(R, stride), (R, stride)
+    # whole rows in shared memory, the streaming grid, rows wider than 128K,
+    # more than 2^24 or fewer than 8192 scores, and invalid shapes: none
+    for R, stride in [(16, 32768), (1024, 16384), (256, 40000), (8, 131073), (200, 90000),
+                      (3, 7), (1, 8191), (0, 1000), (-1, 1000), (4, 0)]:
+        assert L.ds_topk_workspace_size(R, stride, 2048) == 0, (R, stride)
+
+
 def _topk(L, scores=A, stride=1024, rows=4, starts=A, ends=A, k=16, out=A):
     return L.ds_topk_per_row(scores, stride, rows, starts, ends, k, out, None, 0, None)
+
+
+@host_only
+def test_topk_rejects_misaligned_workspace(L):
+    rc = L.ds_topk_per_row(A, 1024, 4, A, A, 16, A, ctypes.c_void_p(0x10010), 1 << 20, None)
+    assert rc == DS_ERR_ALIGN and "workspace" in _err(L)
 
 
 @host_only

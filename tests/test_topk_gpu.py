@@ -8,7 +8,10 @@ lengths, offsets that break 16-byte alignment, rows shorter than, equal to
 and one longer than k, and empty batches. Row widths and batch sizes are
 chosen so that every kernel behind ds_topk_per_row runs: whole rows in
 shared memory (16 or more rows of width <= 32768), the streaming grid (256
-or more rows of up to 65536), and a cluster per row (otherwise).
+or more rows of up to 65536), the grid kernel that spreads every row over
+the whole GPU (the remaining shapes of up to 1024 rows, 131072 wide and
+2^24 scores, when a workspace is given) and a cluster per row (the same
+shapes without a workspace).
 """
 
 import numpy as np
@@ -28,11 +31,11 @@ def ds():
     return ensure_built()
 
 
-def run(ds, scores, starts, ends, k):
+def run(ds, scores, starts, ends, k, workspace=None):
     s = torch.as_tensor(scores, dtype=torch.float32).to(DEV).contiguous()
     a = torch.as_tensor(starts, dtype=torch.int32).to(DEV)
     b = torch.as_tensor(ends, dtype=torch.int32).to(DEV)
-    got = ds.topk_per_row(s, a, b, k)
+    got = ds.topk_per_row(s, a, b, k, workspace=workspace)
     torch.cuda.synchronize()
     return got.cpu().numpy()
 
@@ -258,3 +261,85 @@ def test_large_k_on_every_kernel_exact(ds, rows, stride, k):
     rng = np.random.default_rng(rows * 7 + k)
     s, a, b = _mixed_rows(rng, rows, stride, k)
     check(ds, s, a, b, k)
+
+
+def _grid_run(ds, s, a, b, k, base_offset=0):
+    """Runs the grid kernel with an explicit workspace of stale contents,
+    checking its error word afterwards. base_offset shifts the score matrix
+    by that many floats from a 16-byte boundary; such a matrix takes the
+    kernels that need no workspace (the grid kernel's copies need a 16-byte
+    aligned start)."""
+    R, stride = s.shape
+    need = ds.topk_workspace_size(R, stride, k)
+    assert need > 0, (R, stride)
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device=DEV)   # stale contents
+    flat = torch.empty(R * stride + 4, dtype=torch.float32, device=DEV)
+    dev_s = flat[base_offset:base_offset + R * stride].view(R, stride)
+    dev_s.copy_(torch.as_tensor(s))
+    got = ds.topk_per_row(dev_s, torch.as_tensor(a, dtype=torch.int32).to(DEV),
+                          torch.as_tensor(b, dtype=torch.int32).to(DEV), k, workspace=ws)
+    torch.cuda.synchronize()
+    if base_offset % 4 == 0:
+        assert int(ws[8:12].view(torch.int32).item()) == 0, "a grid wait gave up"
+    return got.cpu().numpy()
+
+
+@pytest.mark.parametrize("rows,stride,k", [(9, 40001, 2048), (8, 100000, 700), (5, 131072, 2048),
+                                           (12, 33000, 64), (15, 32768, 2048), (1, 16384, 2048),
+                                           (40, 70000, 2048), (3, 131072, 16384)])
+def test_grid_kernel_exact(ds, rows, stride, k):
+    # Every refinement case of _mixed_rows, plus ascending and descending rows
+    # and a constant row: lists far longer than one resolve tile.
+    rng = np.random.default_rng(rows * 13 + stride + k)
+    s, a, b = _mixed_rows(rng, rows, stride, k)
+    s[0] = np.arange(stride, dtype=np.float32)
+    if rows > 2:
+        s[2] = -np.arange(stride, dtype=np.float32)
+        a[2], b[2] = 3, stride - 5
+    got = _grid_run(ds, s, a, b, k)
+    want = oracle.topk_per_row(s, a, b, k)
+    assert np.array_equal(got, want), np.nonzero((got != want).any(1))[0][:10].tolist()
+
+
+@pytest.mark.parametrize("base_offset", [1, 2, 3])
+def test_grid_shape_unaligned_score_pointer(ds, base_offset):
+    # A score matrix starting 4, 8 or 12 bytes past a 16-byte boundary, with
+    # a workspace given: the call takes a kernel that reads the scores with
+    # plain loads, and the indices are the same.
+    rng = np.random.default_rng(base_offset)
+    s, a, b = _mixed_rows(rng, 9, 50001, 2048)
+    got = _grid_run(ds, s, a, b, 2048, base_offset=base_offset)
+    assert np.array_equal(got, oracle.topk_per_row(s, a, b, 2048))
+
+
+def test_grid_kernel_equals_workspace_free_kernels(ds):
+    # The TP1 batch shape (128 rows of up to 131072 scores) with and without a
+    # workspace: the grid kernel and the cluster kernel give identical indices,
+    # and the grid kernel repeats bit for bit.
+    c = workload_case("tp1_fp8_decode", device="cuda")
+    assert ds.topk_workspace_size(c.scores.shape[0], c.scores.shape[1], c.k) > 0
+    grid1 = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)
+    grid2 = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k)
+    free = ds.topk_per_row(c.scores, c.row_starts, c.row_ends, c.k, workspace=False)
+    assert torch.equal(grid1, grid2)
+    assert torch.equal(grid1, free)
+
+
+def test_grid_kernel_batch_of_one_row_in_many(ds):
+    # One row alone and inside batches of 7 and 64 neighbours of random
+    # lengths: bitwise the same indices (the rest of the batch changes which
+    # CTAs hold which segments of the row, never the result).
+    rng = np.random.default_rng(21)
+    stride, k = 65536, 2048
+    row = (np.round(rng.standard_normal(stride) * 4) / 4).astype(np.float32)
+    ref = _grid_run(ds, row[None], [0], [60001], k)[0]
+    assert np.array_equal(ref, oracle.topk_per_row(row[None], [0], [60001], k)[0])
+    for B in [7, 64, 255]:
+        s = rng.standard_normal((B, stride)).astype(np.float32)
+        slot = B // 2
+        s[slot] = row
+        a = np.zeros(B, np.int64)
+        b = rng.integers(0, stride + 1, B)
+        b[slot] = 60001
+        got = _grid_run(ds, s, a, b, k)
+        assert np.array_equal(got[slot], ref), B
