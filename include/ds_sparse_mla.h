@@ -119,9 +119,10 @@ int ds_supported_config(int num_heads, int topk, int page_block_size, int d_qk, 
  * over the whole GPU (the grid kernel), or 0 for shapes that another kernel
  * serves without one. Nonzero for batches of at most 256 rows of at most
  * 131072 scores (8192 to 2^24 scores in all) that are neither 16 or more rows
- * of at most 32768 nor 256 or more rows of at most 65536: 256 header bytes, 16 KiB
- * of histogram per row, two small per-row arrays, then 8 bytes per score
- * slot (num_rows * row_stride) for the candidate lists. k does not change it.
+ * of at most 32768 nor 256 or more rows of at most 65536: 256 header bytes,
+ * 16 KiB of histogram per row, two small per-row arrays, then the candidate
+ * lists, 64 KiB for each of the ceil((row_stride + 255) / 8192) segments a
+ * row may have. k does not change it.
  */
 size_t ds_topk_workspace_size(int64_t num_rows, int64_t row_stride, int k);
 

@@ -1220,7 +1220,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
 //      each row of the batch is cut into 8192-score segments starting at
 //      the view row that holds its first score, and the segments are dealt
 //      to the CTAs in contiguous runs. A CTA streams its run through a
-//      5-stage shared-memory ring, one tensor-map box (32 view rows, 32 KiB)
+//      6-stage shared-memory ring, one tensor-map box (32 view rows, 32 KiB)
 //      per segment issued by one thread and completing on the stage's
 //      mbarrier, counts the 12-bit prefixes in shared memory and adds the
 //      counts of each row it touched to that row's histogram in the
@@ -1229,10 +1229,11 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
 //      the barrier), a CTA finds, for each row it touches, the threshold
 //      prefix T (the prefix of the row's k-th largest key) from the row's
 //      histogram, and lists every key whose prefix is at least T with its
-//      position: warps reserve slots in a shared-memory staging list, which
-//      goes to the row's list in the workspace with one global atomic add
-//      per row (a warp whose entries do not fit writes them there itself).
-//      The list's order is arbitrary.
+//      position. Segment j of a row has its own 8192-entry slot of the row's
+//      list: each warp counts its entries, the 32 counts are exchanged across
+//      the block barrier that ends the segment, and every warp writes its
+//      entries at its offset; the segment's count goes to the workspace. No
+//      atomic is involved.
 //   3. One CTA per row resolves the low 20 bits of the threshold on the
 //      list's prefix-T entries (8/8/4-bit histograms, as in the other
 //      kernels), marks the selected positions in a shared-memory bitmap,
@@ -1245,7 +1246,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
 constexpr int kGrThreads = 1024;
 constexpr int kGrPer = 8;                    // scores per thread per segment (two 16-byte groups)
 constexpr int kGrSeg = kGrThreads * kGrPer;  // 8192 scores per segment
-constexpr int kGrStages = 5;                 // ring stages (segments in flight)
+constexpr int kGrStages = 6;                 // ring stages (segments in flight)
 constexpr int kGrView = 256;                 // scores per row of the 2D view
 constexpr int kGrBins = 4096;
 constexpr int kGrMaxRows = 256;
@@ -1256,30 +1257,35 @@ constexpr int kGrWords = (int)(kGrMaxStride / 32);        // bitmap words of a r
 constexpr int kGrWordsPerThread = kGrWords / kGrThreads;  // 4
 constexpr int kGrTileQ = 8;                                // list entries per thread per tile
 constexpr int kGrTile = kGrThreads * kGrTileQ;
-constexpr int kGrStageCap = 4096;                          // staged list entries of one row
 constexpr int kGrOutStage = 8192;                          // output slots staged in shared memory
 constexpr uint32_t kGrNoPos = 0xFFFFFFFFu;
 constexpr long long kGrSpinCycles = 1ll << 31;   // about one second at the top SM clock
-constexpr size_t kGrRingBytes = (size_t)kGrStages * kGrSeg * sizeof(float);   // dynamic, 160 KiB
+constexpr size_t kGrRingBytes = (size_t)kGrStages * kGrSeg * sizeof(float);   // dynamic, 192 KiB
 static_assert(kGrRingBytes >= (2 * kGrWords + kGrOutStage) * sizeof(uint32_t),
               "the bitmaps and the staged output alias the ring");
 
 // Workspace: a 256-byte header (the two barrier counters, then the error
-// word), the row histograms, the list lengths (these three zeroed before each
-// launch), the per-row threshold (prefix T, number of prefix-T keys taken),
-// then the lists, `stride` entries of (key, position) per row.
+// word) and the row histograms (both zeroed before each launch), the entry
+// count of every segment, the per-row threshold (prefix T, number of
+// prefix-T keys taken), then the lists: per row, ns_max slots of 8192
+// (key, position) entries, ns_max = ceil((stride + 255) / 8192) being the
+// most segments a row of the matrix can have.
 constexpr size_t kGrHeader = 256;
+constexpr int kGrMaxSegsPerRow = (int)((kGrMaxStride + kGrView - 1 + kGrSeg - 1) / kGrSeg);   // 17
 __host__ __device__ constexpr size_t gr_align(size_t b) { return (b + 255) & ~size_t(255); }
+__host__ __device__ constexpr int64_t gr_ns_max(int64_t stride) {
+  return (stride + kGrView - 1 + kGrSeg - 1) / kGrSeg;
+}
 __host__ __device__ constexpr size_t gr_hist_off() { return kGrHeader; }
-__host__ __device__ constexpr size_t gr_cnt_off(int64_t R) {
+__host__ __device__ constexpr size_t gr_zero_bytes(int64_t R) {
   return gr_hist_off() + (size_t)R * kGrBins * sizeof(uint32_t);
 }
-__host__ __device__ constexpr size_t gr_zero_bytes(int64_t R) {
-  return gr_cnt_off(R) + gr_align((size_t)R * sizeof(uint32_t));
+__host__ __device__ constexpr size_t gr_segcnt_off(int64_t R) { return gr_zero_bytes(R); }
+__host__ __device__ constexpr size_t gr_info_off(int64_t R, int64_t nsm) {
+  return gr_segcnt_off(R) + gr_align((size_t)(R * nsm) * sizeof(uint32_t));
 }
-__host__ __device__ constexpr size_t gr_info_off(int64_t R) { return gr_zero_bytes(R); }
-__host__ __device__ constexpr size_t gr_list_off(int64_t R) {
-  return gr_info_off(R) + gr_align((size_t)R * sizeof(uint2));
+__host__ __device__ constexpr size_t gr_list_off(int64_t R, int64_t nsm) {
+  return gr_info_off(R, nsm) + gr_align((size_t)R * sizeof(uint2));
 }
 
 struct GridArgs {
@@ -1291,26 +1297,23 @@ struct GridArgs {
   const int32_t* ends;
   int32_t* out;
   uint32_t* hdr;    // [0], [1]: barrier counters; [2]: error word
-  uint32_t* hist;   // [rows][4096]
-  uint32_t* cnt;    // [rows]: list lengths
-  uint2* info;      // [rows]: (T, keys of prefix T to take)
-  uint2* list;      // [rows][stride]: (key, position)
+  uint32_t* hist;     // [rows][4096]
+  uint32_t* segcnt;   // [rows][ns_max]: entries listed from each segment
+  uint2* info;        // [rows]: (T, keys of prefix T to take)
+  uint2* list;        // [rows][ns_max][8192]: (key, position)
+  int32_t ns_max;
 };
 
 struct GridSmem {
   uint32_t seg_off[kGrMaxRows + 1];   // segments before row r; rows with L <= k have none
   int32_t len[kGrMaxRows];
   int32_t g0[kGrMaxRows];             // score element of the row's position 0
-  union {
-    uint32_t hist[kGrBins];        // phase 1: one row's prefix counts
-    uint2 staged[kGrStageCap];     // phase 2: list entries of one row
-  } u;
-  uint32_t h[3][256];   // refinement histograms, one per pass
+  uint32_t hist[kGrBins];        // phase 1: one row's prefix counts
+  uint32_t h[3][256];            // refinement histograms, one per pass
   uint32_t wsum[32];
   uint32_t pick[2];
-  uint32_t fill;        // staged slots reserved
-  uint32_t fit_end;     // first reservation that did not fit (~0: none)
-  uint32_t nflush, gbase;
+  uint32_t wcnt[2][32];          // phase 2: each warp's entries of a segment (by parity)
+  uint32_t segpre[kGrMaxSegsPerRow + 1];   // phase 3: entries before each segment of the row
   alignas(8) uint64_t full[kGrStages];   // ring stage landed (transfer count)
 };
 
@@ -1422,27 +1425,10 @@ __device__ __forceinline__ void gr_flush_hist(const GridArgs& a, GridSmem& sm, i
   __syncthreads();
   uint32_t* const gh = a.hist + (size_t)r * kGrBins;
   for (int i = threadIdx.x; i < kGrBins; i += kGrThreads) {
-    const uint32_t c = sm.u.hist[i];
+    const uint32_t c = sm.hist[i];
     if (c) atomicAdd(gh + i, c);
-    sm.u.hist[i] = 0u;
+    sm.hist[i] = 0u;
   }
-  __syncthreads();
-}
-
-// Moves the staged entries of row r to its list in the workspace.
-__device__ __forceinline__ void gr_flush_list(const GridArgs& a, GridSmem& sm, int r) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t v = sm.fill < sm.fit_end ? sm.fill : sm.fit_end;
-    sm.nflush = v;
-    sm.gbase = v ? atomicAdd(a.cnt + r, v) : 0u;
-    sm.fill = 0u;
-    sm.fit_end = ~0u;
-  }
-  __syncthreads();
-  const uint32_t v = sm.nflush, gb = sm.gbase;
-  uint2* const lr = a.list + (int64_t)r * a.stride + gb;
-  for (uint32_t i = threadIdx.x; i < v; i += kGrThreads) lr[i] = sm.u.staged[i];
   __syncthreads();
 }
 
@@ -1482,39 +1468,54 @@ __device__ __forceinline__ void grid_resolve(const GridArgs& a, GridSmem& sm, ui
     for (int j = tid; j < a.k; j += kGrThreads) orow[j] = j < L ? j : -1;
     return;
   }
-  const uint2* __restrict__ lr = a.list + (int64_t)r * a.stride;
-  // The first tile is read together with the list length (from the part of
-  // the row's list that exists), then trimmed to it.
-  const uint32_t cap = a.stride < kGrTile ? (uint32_t)a.stride : (uint32_t)kGrTile;
-  uint2 e[kGrTileQ];
-#pragma unroll
-  for (int q = 0; q < kGrTileQ; ++q) {
-    const uint32_t i = (uint32_t)(q * kGrThreads + tid);
-    e[q] = i < cap ? __ldcg(lr + i) : make_uint2(0u, kGrNoPos);
-  }
+  // The row's entries: segment j's list slot holds segcnt[r][j] of them.
+  // Entry i of the row (segments in order) is entry i - segpre[j] of the
+  // slot of the segment j with segpre[j] <= i < segpre[j + 1].
+  const int ns = (int)(sm.seg_off[r + 1] - sm.seg_off[r]);   // <= kGrMaxSegsPerRow
   const uint2 inf = __ldcg(a.info + r);
-  uint32_t n = __ldcg(a.cnt + r);
-  if (n > (uint32_t)L) {   // only after a barrier gave up
-    atomicOr(a.hdr + 2, 2u);
+  if (tid < 32) {
+    const int lane = tid;
+    uint32_t c = lane < ns ? __ldcg(a.segcnt + (int64_t)r * a.ns_max + lane) : 0u;
+    if (c > (uint32_t)kGrSeg) c = (uint32_t)kGrSeg;   // only after a wait gave up
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane <= kGrMaxSegsPerRow) sm.segpre[lane] = incl - c;
+  }
+  __syncthreads();
+  uint32_t n = sm.segpre[ns];
+  if (n > (uint32_t)L) {   // only after a wait gave up
+    if (tid == 0) atomicOr(a.hdr + 2, 2u);
     n = (uint32_t)L;
   }
-  auto trim = [&](uint32_t t) {
-#pragma unroll
-    for (int q = 0; q < kGrTileQ; ++q) {
-      const uint32_t i = t * kGrTile + (uint32_t)(q * kGrThreads + tid);
-      if (i >= n || e[q].y >= (uint32_t)L) e[q].y = kGrNoPos;
+  const uint2* __restrict__ lr = a.list + (int64_t)r * a.ns_max * kGrSeg;
+  auto entry = [&](uint32_t i) -> uint2 {
+    int lo = 0, hi = ns;   // segpre[lo] <= i < segpre[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sm.segpre[mid] <= i) lo = mid;
+      else hi = mid;
     }
+    uint2 v = __ldcg(lr + (int64_t)lo * kGrSeg + (i - sm.segpre[lo]));
+    if (v.y >= (uint32_t)L) v.y = kGrNoPos;
+    return v;
   };
+  uint2 e[kGrTileQ];
   auto load_tile = [&](uint32_t t) {
 #pragma unroll
     for (int q = 0; q < kGrTileQ; ++q) {
       const uint32_t i = t * kGrTile + (uint32_t)(q * kGrThreads + tid);
-      e[q] = i < n ? __ldcg(lr + i) : make_uint2(0u, kGrNoPos);
+      e[q] = i < n ? entry(i) : make_uint2(0u, kGrNoPos);
     }
-    trim(t);
   };
   const uint32_t ntiles = (n + kGrTile - 1) / kGrTile;
-  trim(0);
+  // Slots q of a tile hold entries q * 1024 + tid: with one tile, those from
+  // nq on are all empty.
+  const int nq = ntiles > 1 ? kGrTileQ : (int)((n + kGrThreads - 1) / kGrThreads);
+  load_tile(0);
 
   // Threshold state as in the other kernels: prefix P at `shift` dropped
   // bits; `take` of the `cnt` keys with that prefix are selected.
@@ -1528,9 +1529,11 @@ __device__ __forceinline__ void grid_resolve(const GridArgs& a, GridSmem& sm, ui
     for (uint32_t t = 0; t < ntiles; ++t) {
       if (ntiles > 1) load_tile(t);
 #pragma unroll
-      for (int q = 0; q < kGrTileQ; ++q)
+      for (int q = 0; q < kGrTileQ; ++q) {
+        if (q >= nq) break;
         if (e[q].y != kGrNoPos && (e[q].x >> shift) == P)
           atomicAdd(&hs[(e[q].x >> nshift) & dmask], 1u);
+      }
     }
     __syncthreads();
     uint32_t b;
@@ -1544,6 +1547,7 @@ __device__ __forceinline__ void grid_resolve(const GridArgs& a, GridSmem& sm, ui
     if (ntiles > 1) load_tile(t);
 #pragma unroll
     for (int q = 0; q < kGrTileQ; ++q) {
+      if (q >= nq) break;
       if (e[q].y == kGrNoPos) continue;
       const uint32_t hi = e[q].x >> shift;
       const uint32_t bit = 1u << (e[q].y & 31u);
@@ -1625,8 +1629,6 @@ __global__ void __launch_bounds__(kGrThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kGrStages; ++s) mbar_init(&sm.full[s], 1);
     mbar_fence_init();
-    sm.fill = 0u;
-    sm.fit_end = ~0u;
   }
   // Row table: clamped length, start and segment offsets of every row.
   uint32_t ns = 0u;
@@ -1645,7 +1647,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
     sm.g0[tid] = g0;
     if (L > a.k) ns = (uint32_t)(((g0 & (kGrView - 1)) + L + kGrSeg - 1) / kGrSeg);
   }
-  for (int i = tid; i < kGrBins; i += kGrThreads) sm.u.hist[i] = 0u;
+  for (int i = tid; i < kGrBins; i += kGrThreads) sm.hist[i] = 0u;
   uint32_t S;
   const uint32_t ex = block_exclusive_scan_nt<kGrThreads>(ns, sm.wsum, S);
   if (tid <= R) sm.seg_off[tid] = ex;   // thread R's exclusive sum is the total
@@ -1701,7 +1703,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
     take_stage(seg, valid, x);
 #pragma unroll
     for (int q = 0; q < kGrPer; ++q)
-      if ((valid >> q) & 1u) atomicAdd(&sm.u.hist[score_key(x[q]) >> 20], 1u);
+      if ((valid >> q) & 1u) atomicAdd(&sm.hist[score_key(x[q]) >> 20], 1u);
     release_stage(seg);
   }
   if (cur >= 0) gr_flush_hist(a, sm, cur);
@@ -1711,29 +1713,44 @@ __global__ void __launch_bounds__(kGrThreads, 1)
   grid_barrier(a.hdr, G, a.hdr + 2);
 
   // Phase 2: threshold prefix of each row touched, then the lists.
+  const int warp = tid >> 5;
+  uint32_t wpar = 0u;
   pc.r = -1;
   cur = -1;
-  uint32_t lo_key = 0u;   // a key's prefix is at least T iff key >= lo_key
+  // A key's prefix is at least T iff key >= lo_key. For 8 <= T <= 0xFF8
+  // (0xFF8 is the bin of +inf, the highest a key reaches) that is the float
+  // comparison x >= lo_x, lo_x being the float whose key is lo_key: keys are
+  // monotone in the float order, -0 and +0 compare equal as they should, and
+  // NaN (key 0) compares false. Outside that range lo_x would be a NaN
+  // pattern; such rows compare keys.
+  uint32_t lo_key = 0u;
+  float lo_x = 0.f;
+  bool by_float = false;
   for (uint32_t seg = sb; seg < se; ++seg) {
     gr_locate(sm, a, seg, pc);
     if (pc.r != cur) {
-      if (cur >= 0) gr_flush_list(a, sm, cur);
       cur = pc.r;
       gr_threshold(a, sm, cur);
       const uint32_t T = sm.pick[0];
       if (pc.j == 0 && tid == 0) a.info[cur] = make_uint2(T, k - sm.pick[1]);
       lo_key = T << 20;
+      by_float = T >= 8u && T <= 0xFF8u;
+      lo_x = __uint_as_float((lo_key & 0x80000000u) ? (lo_key & 0x7FFFFFFFu) : ~lo_key);
     }
     const uint32_t valid = gr_valid(pc, tid);
     float x[kGrPer];
     take_stage(seg, valid, x);
-    uint32_t kk[kGrPer];
     uint32_t m = 0u;
+    if (by_float) {
 #pragma unroll
-    for (int q = 0; q < kGrPer; ++q) {
-      kk[q] = score_key(x[q]);
-      if (((valid >> q) & 1u) && kk[q] >= lo_key) m |= 1u << q;
+      for (int q = 0; q < kGrPer; ++q)
+        if (x[q] >= lo_x) m |= 1u << q;
+    } else {
+#pragma unroll
+      for (int q = 0; q < kGrPer; ++q)
+        if (score_key(x[q]) >= lo_key) m |= 1u << q;
     }
+    m &= valid;
     const uint32_t cm = __popc(m);
     uint32_t incl = cm;
 #pragma unroll
@@ -1741,35 +1758,30 @@ __global__ void __launch_bounds__(kGrThreads, 1)
       const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    const uint32_t wt = __shfl_sync(0xffffffffu, incl, 31);
-    if (wt != 0u) {
-      uint32_t base = 0u;
-      if (lane == 31) base = atomicAdd(&sm.fill, wt);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      const uint32_t p0 = (uint32_t)(pc.A + 4 * tid - pc.g0);   // position of score q = 0
-      if (base + wt <= (uint32_t)kGrStageCap) {
-        uint32_t o = base + incl - cm;
+    if (lane == 31) sm.wcnt[wpar][warp] = incl;
+    release_stage(seg);   // its barrier also publishes the warp counts
+    // This warp's offset in the segment's slot: the counts of the warps
+    // before it.
+    const uint32_t wc = sm.wcnt[wpar][lane];
+    uint32_t winc = wc;
 #pragma unroll
-        for (int q = 0; q < kGrPer; ++q)
-          if ((m >> q) & 1u)
-            sm.u.staged[o++] = make_uint2(kk[q], p0 + (uint32_t)(4096 * (q >> 2) + (q & 3)));
-      } else {
-        // Staging full: this warp's entries go to the row's list directly.
-        uint32_t gb = 0u;
-        if (lane == 31) {
-          atomicMin(&sm.fit_end, base);
-          gb = atomicAdd(a.cnt + cur, wt);
-        }
-        uint32_t o = __shfl_sync(0xffffffffu, gb, 31) + incl - cm;
-        uint2* const lr = a.list + (int64_t)cur * a.stride;
-#pragma unroll
-        for (int q = 0; q < kGrPer; ++q)
-          if ((m >> q) & 1u) lr[o++] = make_uint2(kk[q], p0 + (uint32_t)(4096 * (q >> 2) + (q & 3)));
-      }
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += y;
     }
-    release_stage(seg);
+    const uint32_t woff = __shfl_sync(0xffffffffu, winc - wc, warp);
+    if (tid == 31) a.segcnt[(int64_t)cur * a.ns_max + pc.j] = winc;   // the segment's total
+    if (m) {
+      uint2* const ls = a.list + ((int64_t)cur * a.ns_max + pc.j) * kGrSeg;
+      const uint32_t p0 = (uint32_t)(pc.A + 4 * tid - pc.g0);   // position of score q = 0
+      uint32_t o = woff + incl - cm;
+#pragma unroll
+      for (int q = 0; q < kGrPer; ++q)
+        if ((m >> q) & 1u)
+          ls[o++] = make_uint2(score_key(x[q]), p0 + (uint32_t)(4096 * (q >> 2) + (q & 3)));
+    }
+    wpar ^= 1u;
   }
-  if (cur >= 0) gr_flush_list(a, sm, cur);
   if (late && tid == 0) atomicOr(a.hdr + 2, 4u);
 
   // Every copy issued has been waited for: the ring's space becomes the two
@@ -1802,7 +1814,8 @@ bool topk_grid_shape(int64_t rows, int64_t stride) {
 
 size_t topk_workspace_bytes(int64_t rows, int64_t stride) {
   if (!topk_grid_shape(rows, stride)) return 0;
-  return gr_list_off(rows) + (size_t)rows * (size_t)stride * sizeof(uint2);
+  const int64_t nsm = gr_ns_max(stride);
+  return gr_list_off(rows, nsm) + (size_t)(rows * nsm) * kGrSeg * sizeof(uint2);
 }
 
 namespace {
@@ -1862,10 +1875,12 @@ cudaError_t launch_topk_grid(const float* scores, int64_t stride, int64_t rows,
   a.ends = ends;
   a.out = out;
   a.hdr = reinterpret_cast<uint32_t*>(ws);
+  const int64_t nsm = gr_ns_max(stride);
   a.hist = reinterpret_cast<uint32_t*>(ws + gr_hist_off());
-  a.cnt = reinterpret_cast<uint32_t*>(ws + gr_cnt_off(rows));
-  a.info = reinterpret_cast<uint2*>(ws + gr_info_off(rows));
-  a.list = reinterpret_cast<uint2*>(ws + gr_list_off(rows));
+  a.segcnt = reinterpret_cast<uint32_t*>(ws + gr_segcnt_off(rows));
+  a.info = reinterpret_cast<uint2*>(ws + gr_info_off(rows, nsm));
+  a.list = reinterpret_cast<uint2*>(ws + gr_list_off(rows, nsm));
+  a.ns_max = (int32_t)nsm;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kGrThreads);
