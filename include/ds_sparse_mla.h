@@ -120,9 +120,9 @@ int ds_supported_config(int num_heads, int topk, int page_block_size, int d_qk, 
  * serves without one. Nonzero for batches of at most 256 rows of at most
  * 131072 scores (8192 to 2^24 scores in all) that are neither 16 or more rows
  * of at most 32768 nor 256 or more rows of at most 65536: 256 header bytes,
- * 16 KiB of histogram per row, two small per-row arrays, then the candidate
- * lists, 64 KiB for each of the ceil((row_stride + 255) / 8192) segments a
- * row may have. k does not change it.
+ * then 64 KiB of candidate list and 8 bytes of bookkeeping for each of the
+ * ceil((row_stride + 255) / 8192) segments a row may have, per row. k does
+ * not change it.
  */
 size_t ds_topk_workspace_size(int64_t num_rows, int64_t row_stride, int k);
 
@@ -160,16 +160,16 @@ size_t ds_sparse_mla_workspace_size(int64_t num_rows, int num_heads, int k);
  *
  *  workspace   NULL, or 256-byte aligned device memory of workspace_bytes.
  *              With at least ds_topk_workspace_size() bytes (when that is
- *              nonzero) and scores 16-byte aligned, the grid kernel runs: one cooperative launch whose
- *              CTAs are all resident, preceded by a zero fill of the
- *              workspace's first bytes (so its contents need no
- *              initialisation); otherwise a kernel that needs no workspace
- *              runs. The output is identical either way. After the grid
- *              kernel, the int32 at byte offset 8 of the workspace is 0; a
- *              nonzero value means one of its bounded inter-CTA waits gave
- *              up (not expected: the launch keeps every CTA resident) and
- *              idx_out is unspecified. Concurrent calls need separate
- *              workspaces.
+ *              nonzero) and scores 16-byte aligned, the grid kernel runs:
+ *              one cooperative launch whose CTAs are all resident, preceded
+ *              by a zero fill of the workspace's first 256 bytes (so its
+ *              contents need no initialisation); otherwise a kernel that
+ *              needs no workspace runs. The output is identical either way.
+ *              After the grid kernel, the int32 at byte offset 8 of the
+ *              workspace is 0; a nonzero value means one of its bounded
+ *              waits gave up (not expected: the launch keeps every CTA
+ *              resident) and idx_out is unspecified. Concurrent calls need
+ *              separate workspaces.
  */
 int ds_topk_per_row(const float* scores, int64_t row_stride, int64_t num_rows,
                     const int32_t* row_starts, const int32_t* row_ends, int k,

@@ -39,6 +39,7 @@
 // Its output slot is (#greater before it) + min(#equal before it, take).
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -1212,36 +1213,37 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
 
 // ---------------------------------------------------------------------------
 // Grid variant, for up to 256 rows of up to 131072 scores (8192 to 2^24
-// scores in all): every row is spread over the whole GPU. One cooperative
-// launch of one 1024-thread CTA per SM, all resident at once, runs three
-// phases separated by two grid barriers (a counter in the workspace, waited
-// on with a bounded spin):
+// scores in all): every row is spread over the whole GPU and read once. One
+// cooperative launch of one 1024-thread CTA per SM, all resident at once,
+// runs two phases separated by one grid barrier (a counter in the
+// workspace, waited on with a bounded spin):
 //   1. The score matrix (16-byte aligned) is viewed as rows of 256 scores;
 //      each row of the batch is cut into 8192-score segments starting at
 //      the view row that holds its first score, and the segments are dealt
 //      to the CTAs in contiguous runs. A CTA streams its run through a
 //      6-stage shared-memory ring, one tensor-map box (32 view rows, 32 KiB)
 //      per segment issued by one thread and completing on the stage's
-//      mbarrier, counts the 12-bit prefixes in shared memory and adds the
-//      counts of each row it touched to that row's histogram in the
-//      workspace (zeroed before the launch).
-//   2. Streaming its run again (from L2; the first copies are issued before
-//      the barrier), a CTA finds, for each row it touches, the threshold
-//      prefix T (the prefix of the row's k-th largest key) from the row's
-//      histogram, and lists every key whose prefix is at least T with its
-//      position. Segment j of a row has its own 8192-entry slot of the row's
-//      list: each warp counts its entries, the 32 counts are exchanged across
-//      the block barrier that ends the segment, and every warp writes its
-//      entries at its offset; the segment's count goes to the workspace. No
-//      atomic is involved.
-//   3. One CTA per row resolves the low 20 bits of the threshold on the
-//      list's prefix-T entries (8/8/4-bit histograms, as in the other
-//      kernels), marks the selected positions in a shared-memory bitmap,
-//      settles ties at the full key in a second bitmap (the lowest positions
-//      win, by one block scan) and writes the positions in ascending order
-//      (staged in shared memory, then stored contiguously).
-// The result is the same set as every other kernel's: the list's order only
-// changes which thread marks which bit.
+//      mbarrier. On the first segment of each row it touches (n in-row
+//      scores) it takes a bound B: the 12-bit prefix bin holding the
+//      segment's (2 k n / L + 32)-th largest key (every key when n is
+//      smaller), a generous estimate of where the row's k-th largest key
+//      lies. It then lists every score of its part of the row whose key is
+//      at least B << 20, with its position: segment j of a row has its own
+//      8192-entry slot of the row's list, warps exchange their counts across
+//      the block barrier that ends the segment and write at their offsets,
+//      and the segment's count and bound go to the workspace.
+//   2. One CTA per row takes M, the largest bound any segment of the row
+//      used. If at least k listed keys are >= M, the row's k-th largest key
+//      is >= M >= every segment's bound, so every key of the top k was
+//      listed, and the top k of the listed keys >= M is the answer. Otherwise
+//      (rows whose first segments misjudge the rest, such as descending
+//      rows) the CTA takes the whole row from the score matrix instead. It
+//      selects by 12/8/8/4-bit histograms (ties at the full key take the
+//      lowest positions), marks the selected positions in a shared-memory
+//      bitmap and writes them in ascending order (staged in shared memory,
+//      then stored contiguously).
+// The result is the same set as every other kernel's: which scores are
+// listed, and in which order, only changes the work.
 
 constexpr int kGrThreads = 1024;
 constexpr int kGrPer = 8;                    // scores per thread per segment (two 16-byte groups)
@@ -1255,7 +1257,7 @@ constexpr int64_t kGrMinScores = kGrSeg;
 constexpr int64_t kGrMaxScores = int64_t(1) << 24;
 constexpr int kGrWords = (int)(kGrMaxStride / 32);        // bitmap words of a row
 constexpr int kGrWordsPerThread = kGrWords / kGrThreads;  // 4
-constexpr int kGrTileQ = 8;                                // list entries per thread per tile
+constexpr int kGrTileQ = 8;                                // entries per thread per tile
 constexpr int kGrTile = kGrThreads * kGrTileQ;
 constexpr int kGrOutStage = 8192;                          // output slots staged in shared memory
 constexpr uint32_t kGrNoPos = 0xFFFFFFFFu;
@@ -1264,28 +1266,23 @@ constexpr size_t kGrRingBytes = (size_t)kGrStages * kGrSeg * sizeof(float);   //
 static_assert(kGrRingBytes >= (2 * kGrWords + kGrOutStage) * sizeof(uint32_t),
               "the bitmaps and the staged output alias the ring");
 
-// Workspace: a 256-byte header (the two barrier counters, then the error
-// word) and the row histograms (both zeroed before each launch), the entry
-// count of every segment, the per-row threshold (prefix T, number of
-// prefix-T keys taken), then the lists: per row, ns_max slots of 8192
-// (key, position) entries, ns_max = ceil((stride + 255) / 8192) being the
-// most segments a row of the matrix can have.
+// Workspace: a 256-byte header (the barrier counter, then the error word;
+// zeroed before each launch), the entry count and the bound of every
+// segment, then the lists: per row, ns_max slots of 8192 (key, position)
+// entries, ns_max = ceil((stride + 255) / 8192) being the most segments a
+// row of the matrix can have.
 constexpr size_t kGrHeader = 256;
 constexpr int kGrMaxSegsPerRow = (int)((kGrMaxStride + kGrView - 1 + kGrSeg - 1) / kGrSeg);   // 17
 __host__ __device__ constexpr size_t gr_align(size_t b) { return (b + 255) & ~size_t(255); }
 __host__ __device__ constexpr int64_t gr_ns_max(int64_t stride) {
   return (stride + kGrView - 1 + kGrSeg - 1) / kGrSeg;
 }
-__host__ __device__ constexpr size_t gr_hist_off() { return kGrHeader; }
-__host__ __device__ constexpr size_t gr_zero_bytes(int64_t R) {
-  return gr_hist_off() + (size_t)R * kGrBins * sizeof(uint32_t);
-}
-__host__ __device__ constexpr size_t gr_segcnt_off(int64_t R) { return gr_zero_bytes(R); }
-__host__ __device__ constexpr size_t gr_info_off(int64_t R, int64_t nsm) {
-  return gr_segcnt_off(R) + gr_align((size_t)(R * nsm) * sizeof(uint32_t));
+__host__ __device__ constexpr size_t gr_segcnt_off() { return kGrHeader; }
+__host__ __device__ constexpr size_t gr_segbound_off(int64_t R, int64_t nsm) {
+  return gr_segcnt_off() + gr_align((size_t)(R * nsm) * sizeof(uint32_t));
 }
 __host__ __device__ constexpr size_t gr_list_off(int64_t R, int64_t nsm) {
-  return gr_info_off(R, nsm) + gr_align((size_t)R * sizeof(uint2));
+  return gr_segbound_off(R, nsm) + gr_align((size_t)(R * nsm) * sizeof(uint32_t));
 }
 
 struct GridArgs {
@@ -1296,11 +1293,10 @@ struct GridArgs {
   const int32_t* starts;
   const int32_t* ends;
   int32_t* out;
-  uint32_t* hdr;    // [0], [1]: barrier counters; [2]: error word
-  uint32_t* hist;     // [rows][4096]
-  uint32_t* segcnt;   // [rows][ns_max]: entries listed from each segment
-  uint2* info;        // [rows]: (T, keys of prefix T to take)
-  uint2* list;        // [rows][ns_max][8192]: (key, position)
+  uint32_t* hdr;        // [0]: barrier counter; [2]: error word
+  uint32_t* segcnt;     // [rows][ns_max]: entries listed from each segment
+  uint32_t* segbound;   // [rows][ns_max]: the key bound each segment listed from
+  uint2* list;          // [rows][ns_max][8192]: (key, position)
   int32_t ns_max;
 };
 
@@ -1308,14 +1304,18 @@ struct GridSmem {
   uint32_t seg_off[kGrMaxRows + 1];   // segments before row r; rows with L <= k have none
   int32_t len[kGrMaxRows];
   int32_t g0[kGrMaxRows];             // score element of the row's position 0
-  uint32_t hist[kGrBins];        // phase 1: one row's prefix counts
-  uint32_t h[3][256];            // refinement histograms, one per pass
+  alignas(16) uint32_t hist[kGrBins];   // 12-bit prefix counts; zero between uses (read as uint4)
+  uint32_t h[3][256];                 // refinement histograms, one per pass
   uint32_t wsum[32];
-  uint32_t pick[2];
-  uint32_t wcnt[2][32];          // phase 2: each warp's entries of a segment (by parity)
-  uint32_t segpre[kGrMaxSegsPerRow + 1];   // phase 3: entries before each segment of the row
+  uint32_t pick[3];
+  uint32_t wcnt[2][32];               // each warp's entries of a segment (by parity)
+  uint32_t segpre[kGrMaxSegsPerRow + 1];   // phase 2: entries before each segment of the row
+  uint32_t mkey;                      // phase 2: the row's bound M
   alignas(8) uint64_t full[kGrStages];   // ring stage landed (transfer count)
 };
+
+static_assert(offsetof(GridSmem, hist) % 16 == 0, "the histogram is read 16 bytes at a time");
+static_assert(offsetof(GridSmem, full) % 8 == 0, "mbarriers are 8-byte aligned");
 
 // Every CTA arrives once; thread 0 waits until all `target` CTAs have, for at
 // most kGrSpinCycles, after which it sets the error word and goes on (the
@@ -1419,45 +1419,34 @@ __device__ __forceinline__ void gr_scores(const float* ring_stage, const GrSeg& 
   }
 }
 
-// Adds the shared-memory counts of row r to its histogram in the workspace
-// and clears them.
-__device__ __forceinline__ void gr_flush_hist(const GridArgs& a, GridSmem& sm, int r) {
-  __syncthreads();
-  uint32_t* const gh = a.hist + (size_t)r * kGrBins;
-  for (int i = threadIdx.x; i < kGrBins; i += kGrThreads) {
-    const uint32_t c = sm.hist[i];
-    if (c) atomicAdd(gh + i, c);
-    sm.hist[i] = 0u;
-  }
-  __syncthreads();
-}
-
-// Threshold prefix of row r from its histogram: sm.pick = (T, number of keys
-// whose prefix is above T). Thread t reads bins 4095 - 4t - q, q = 0..3.
+// Picks, among the 4096 bins of sm.hist (descending bin order), the bin
+// holding the `take`-th largest key: sm.pick = (bin, keys above the bin,
+// keys in the bin). Thread t reads (and clears) bins 4095 - 4t - q,
+// q = 0..3. Ends with a block barrier.
 constexpr int kGrBinsPerThread = kGrBins / kGrThreads;
-static_assert(kGrBinsPerThread == 4, "one 16-byte load of bins per thread");
-__device__ __forceinline__ void gr_threshold(const GridArgs& a, GridSmem& sm, int r) {
+static_assert(kGrBinsPerThread == 4, "one 16-byte read of bins per thread");
+__device__ __forceinline__ void gr_pick4096(GridSmem& sm, uint32_t take) {
   const int tid = threadIdx.x;
-  const uint32_t k = (uint32_t)a.k;
-  const uint32_t* gh = a.hist + (size_t)r * kGrBins;
-  const uint4 b4 = __ldcg(reinterpret_cast<const uint4*>(gh + kGrBins - 4 - 4 * tid));
+  uint4* const p4 = reinterpret_cast<uint4*>(sm.hist + kGrBins - 4 - 4 * tid);
+  const uint4 b4 = *p4;
+  *p4 = make_uint4(0u, 0u, 0u, 0u);
   const uint32_t c[4] = {b4.w, b4.z, b4.y, b4.x};
-  const uint32_t mine = c[0] + c[1] + c[2] + c[3];
   uint32_t tot;
-  uint32_t above = block_exclusive_scan_nt<kGrThreads>(mine, sm.wsum, tot);
+  uint32_t above = block_exclusive_scan_nt<kGrThreads>(c[0] + c[1] + c[2] + c[3], sm.wsum, tot);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    if (above < k && k <= above + c[q]) {
+    if (above < take && take <= above + c[q]) {
       sm.pick[0] = (uint32_t)(kGrBins - 1 - 4 * tid - q);
       sm.pick[1] = above;
+      sm.pick[2] = c[q];
     }
     above += c[q];
   }
   __syncthreads();
 }
 
-// Phase 3 for row r. On entry the bitmaps and refinement histograms are
-// zero; they are zero again on return.
+// Phase 2 for row r. On entry the bitmaps, sm.hist and the refinement
+// histograms are zero; they are zero again on return.
 __device__ __forceinline__ void grid_resolve(const GridArgs& a, GridSmem& sm, uint32_t* sel,
                                              uint32_t* tie, int32_t* out_s, int r) {
   const int tid = threadIdx.x;
@@ -1472,27 +1461,33 @@ __device__ __forceinline__ void grid_resolve(const GridArgs& a, GridSmem& sm, ui
   // Entry i of the row (segments in order) is entry i - segpre[j] of the
   // slot of the segment j with segpre[j] <= i < segpre[j + 1].
   const int ns = (int)(sm.seg_off[r + 1] - sm.seg_off[r]);   // <= kGrMaxSegsPerRow
-  const uint2 inf = __ldcg(a.info + r);
   if (tid < 32) {
     const int lane = tid;
-    uint32_t c = lane < ns ? __ldcg(a.segcnt + (int64_t)r * a.ns_max + lane) : 0u;
+    uint32_t c = 0u, bnd = 0u;
+    if (lane < ns) {
+      c = __ldcg(a.segcnt + (int64_t)r * a.ns_max + lane);
+      bnd = __ldcg(a.segbound + (int64_t)r * a.ns_max + lane);
+    }
     if (c > (uint32_t)kGrSeg) c = (uint32_t)kGrSeg;   // only after a wait gave up
     uint32_t incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
+      bnd = max(bnd, __shfl_xor_sync(0xffffffffu, bnd, o));
     }
     if (lane <= kGrMaxSegsPerRow) sm.segpre[lane] = incl - c;
+    if (lane == 0) sm.mkey = bnd;
   }
   __syncthreads();
   uint32_t n = sm.segpre[ns];
-  if (n > (uint32_t)L) {   // only after a wait gave up
-    if (tid == 0) atomicOr(a.hdr + 2, 2u);
-    n = (uint32_t)L;
-  }
+  uint32_t mkey = sm.mkey;
+  if (n > (uint32_t)L) n = (uint32_t)L;   // only after a wait gave up
   const uint2* __restrict__ lr = a.list + (int64_t)r * a.ns_max * kGrSeg;
+  const float* __restrict__ srow = a.scores + sm.g0[r];
+  bool whole = false;   // entries from the score row itself
   auto entry = [&](uint32_t i) -> uint2 {
+    if (whole) return make_uint2(score_key(srow[i]), i);
     int lo = 0, hi = ns;   // segpre[lo] <= i < segpre[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -1504,22 +1499,51 @@ __device__ __forceinline__ void grid_resolve(const GridArgs& a, GridSmem& sm, ui
     return v;
   };
   uint2 e[kGrTileQ];
+  // Slot q of tile t holds entry t * 8192 + q * 1024 + tid; entries below
+  // the bound M are not candidates.
   auto load_tile = [&](uint32_t t) {
 #pragma unroll
     for (int q = 0; q < kGrTileQ; ++q) {
       const uint32_t i = t * kGrTile + (uint32_t)(q * kGrThreads + tid);
       e[q] = i < n ? entry(i) : make_uint2(0u, kGrNoPos);
+      if (e[q].x < mkey) e[q].y = kGrNoPos;
     }
   };
-  const uint32_t ntiles = (n + kGrTile - 1) / kGrTile;
-  // Slots q of a tile hold entries q * 1024 + tid: with one tile, those from
-  // nq on are all empty.
+  uint32_t ntiles = (n + kGrTile - 1) / kGrTile;
+  uint32_t mine = 0u;
+  for (uint32_t t = 0; t < ntiles; ++t) {
+    load_tile(t);
+#pragma unroll
+    for (int q = 0; q < kGrTileQ; ++q) mine += e[q].y != kGrNoPos;
+  }
+  uint32_t cand;
+  (void)block_exclusive_scan_nt<kGrThreads>(mine, sm.wsum, cand);
+  if (cand < k) {
+    // Fewer than k listed keys reach M: the lists may miss some of the top
+    // k, so the row is taken whole.
+    whole = true;
+    n = (uint32_t)L;
+    mkey = 0u;
+    cand = n;
+    ntiles = (n + kGrTile - 1) / kGrTile;
+  }
+  if (ntiles == 1 && whole) load_tile(0);   // (the lists' single tile is loaded already)
   const int nq = ntiles > 1 ? kGrTileQ : (int)((n + kGrThreads - 1) / kGrThreads);
-  load_tile(0);
 
-  // Threshold state as in the other kernels: prefix P at `shift` dropped
-  // bits; `take` of the `cnt` keys with that prefix are selected.
-  uint32_t P = inf.x, take = inf.y, cnt = n - (k - inf.y);
+  // The top 12 bits, then 8/8/4 as in the other kernels: prefix P at
+  // `shift` dropped bits; `take` of the `cnt` candidates with that prefix are
+  // selected.
+  for (uint32_t t = 0; t < ntiles; ++t) {
+    if (ntiles > 1) load_tile(t);
+#pragma unroll
+    for (int q = 0; q < kGrTileQ; ++q) {
+      if (q >= nq) break;
+      if (e[q].y != kGrNoPos) atomicAdd(&sm.hist[e[q].x >> 20], 1u);
+    }
+  }
+  __syncthreads();
+  gr_pick4096(sm, k);
+  uint32_t P = sm.pick[0], take = k - sm.pick[1], cnt = sm.pick[2];
   int shift = 20;
   for (int pass = 0; pass < 3 && cnt != take; ++pass) {
     const int width = pass < 2 ? 8 : 4;
@@ -1621,7 +1645,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
     topk_grid_kernel(const __grid_constant__ CUtensorMap smap, const GridArgs a) {
   __shared__ GridSmem sm;
   extern __shared__ __align__(128) float gr_ring[];   // [kGrStages][kGrSeg]
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.rows;
   const uint32_t G = gridDim.x;
   const uint32_t k = (uint32_t)a.k;
@@ -1657,89 +1681,64 @@ __global__ void __launch_bounds__(kGrThreads, 1)
   const int32_t ncov = (int32_t)(((int64_t)R * a.stride) & ~int64_t(kGrView - 1));
 
   // The ring: segment sb + i goes to stage i % kGrStages. Thread 0 fills the
-  // stages; every thread waits for a stage's copies, reads its 16 bytes, and
-  // after the block barrier that ends each segment thread 0 refills the
+  // stages; every thread waits for a stage's copies and reads its scores,
+  // and after the block barrier that ends each segment thread 0 refills the
   // stage with the segment kGrStages further on. `par` holds the parity of
   // each stage's next phase.
   GrSeg ic, pc;
   uint32_t par = 0u;
   bool late = false;   // a ring wait gave up
-  auto prime = [&]() {
-    if (tid == 0) {
-      ic.r = -1;
-      for (int s = 0; s < kGrStages && sb + s < se; ++s) {
-        gr_locate(sm, a, sb + s, ic);
-        gr_issue(&smap, sm, gr_ring, ic, s);
-      }
+  if (tid == 0) {
+    ic.r = -1;
+    for (int s = 0; s < kGrStages && sb + s < se; ++s) {
+      gr_locate(sm, a, sb + s, ic);
+      gr_issue(&smap, sm, gr_ring, ic, s);
     }
-  };
-  auto take_stage = [&](uint32_t seg, uint32_t valid, float (&x)[kGrPer]) {
-    const int st = (int)((seg - sb) % kGrStages);
-    if (!mbar_wait(&sm.full[st], (par >> st) & 1u)) late = true;
-    par ^= 1u << st;
-    gr_scores(gr_ring + st * kGrSeg, pc, tid, valid, ncov, a.scores, x);
-  };
-  auto release_stage = [&](uint32_t seg) {
-    __syncthreads();   // every thread has read the stage
-    const uint32_t nx = seg + kGrStages;
-    if (tid == 0 && nx < se) {
-      gr_locate(sm, a, nx, ic);
-      gr_issue(&smap, sm, gr_ring, ic, (int)((nx - sb) % kGrStages));
-    }
-  };
+  }
 
-  // Phase 1: 12-bit prefix counts.
-  prime();
+  // Phase 1.
   pc.r = -1;
   int cur = -1;
-  for (uint32_t seg = sb; seg < se; ++seg) {
-    gr_locate(sm, a, seg, pc);
-    if (pc.r != cur) {
-      if (cur >= 0) gr_flush_hist(a, sm, cur);
-      cur = pc.r;
-    }
-    const uint32_t valid = gr_valid(pc, tid);
-    float x[kGrPer];
-    take_stage(seg, valid, x);
-#pragma unroll
-    for (int q = 0; q < kGrPer; ++q)
-      if ((valid >> q) & 1u) atomicAdd(&sm.hist[score_key(x[q]) >> 20], 1u);
-    release_stage(seg);
-  }
-  if (cur >= 0) gr_flush_hist(a, sm, cur);
-
-  // The scores are read-only: phase 2's first copies go out before the wait.
-  prime();
-  grid_barrier(a.hdr, G, a.hdr + 2);
-
-  // Phase 2: threshold prefix of each row touched, then the lists.
-  const int warp = tid >> 5;
-  uint32_t wpar = 0u;
-  pc.r = -1;
-  cur = -1;
-  // A key's prefix is at least T iff key >= lo_key. For 8 <= T <= 0xFF8
-  // (0xFF8 is the bin of +inf, the highest a key reaches) that is the float
-  // comparison x >= lo_x, lo_x being the float whose key is lo_key: keys are
-  // monotone in the float order, -0 and +0 compare equal as they should, and
-  // NaN (key 0) compares false. Outside that range lo_x would be a NaN
-  // pattern; such rows compare keys.
+  // A key is listed iff key >= lo_key. For 8 <= B <= 0xFF8 (0xFF8 is the
+  // bin of +inf, the highest a key reaches) that is the float comparison
+  // x >= lo_x, lo_x being the float whose key is lo_key: keys are monotone
+  // in the float order, -0 and +0 compare equal as they should, and NaN (key
+  // 0) compares false. Outside that range lo_x would be a NaN pattern; such
+  // bounds compare keys.
   uint32_t lo_key = 0u;
   float lo_x = 0.f;
   bool by_float = false;
+  uint32_t wpar = 0u;
   for (uint32_t seg = sb; seg < se; ++seg) {
     gr_locate(sm, a, seg, pc);
-    if (pc.r != cur) {
-      cur = pc.r;
-      gr_threshold(a, sm, cur);
-      const uint32_t T = sm.pick[0];
-      if (pc.j == 0 && tid == 0) a.info[cur] = make_uint2(T, k - sm.pick[1]);
-      lo_key = T << 20;
-      by_float = T >= 8u && T <= 0xFF8u;
-      lo_x = __uint_as_float((lo_key & 0x80000000u) ? (lo_key & 0x7FFFFFFFu) : ~lo_key);
-    }
+    const bool first = pc.r != cur;
+    cur = pc.r;
     const uint32_t valid = gr_valid(pc, tid);
     float x[kGrPer];
-    take_stage(seg, valid, x);
+    {
+      const int st = (int)((seg - sb) % kGrStages);
+      if (!mbar_wait(&sm.full[st], (par >> st) & 1u)) late = true;
+      par ^= 1u << st;
+      gr_scores(gr_ring + st * kGrSeg, pc, tid, valid, ncov, a.scores, x);
+    }
+    if (first) {
+      // The bound from this segment's n in-row scores: the bin of its
+      // (2 k n / L + 32)-th largest key.
+#pragma unroll
+      for (int q = 0; q < kGrPer; ++q)
+        if ((valid >> q) & 1u) atomicAdd(&sm.hist[score_key(x[q]) >> 20], 1u);
+      __syncthreads();
+      const int32_t lo_e = pc.A > pc.g0 ? pc.A : pc.g0;
+      const int32_t hi_e = pc.A + kGrSeg < pc.gend ? pc.A + kGrSeg : pc.gend;
+      const uint32_t nseg = (uint32_t)(hi_e - lo_e);
+      uint64_t t1 = 2ull * k * nseg / (uint64_t)(pc.gend - pc.g0) + 32u;
+      if (t1 > nseg) t1 = nseg;
+      gr_pick4096(sm, (uint32_t)t1);
+      const uint32_t B = sm.pick[0];
+      lo_key = B << 20;
+      by_float = B >= 8u && B <= 0xFF8u;
+      lo_x = __uint_as_float((lo_key & 0x80000000u) ? (lo_key & 0x7FFFFFFFu) : ~lo_key);
+    }
     uint32_t m = 0u;
     if (by_float) {
 #pragma unroll
@@ -1759,7 +1758,14 @@ __global__ void __launch_bounds__(kGrThreads, 1)
       if (lane >= o) incl += y;
     }
     if (lane == 31) sm.wcnt[wpar][warp] = incl;
-    release_stage(seg);   // its barrier also publishes the warp counts
+    __syncthreads();   // every thread has read the stage; the warp counts are out
+    {
+      const uint32_t nx = seg + kGrStages;
+      if (tid == 0 && nx < se) {
+        gr_locate(sm, a, nx, ic);
+        gr_issue(&smap, sm, gr_ring, ic, (int)((nx - sb) % kGrStages));
+      }
+    }
     // This warp's offset in the segment's slot: the counts of the warps
     // before it.
     const uint32_t wc = sm.wcnt[wpar][lane];
@@ -1770,7 +1776,10 @@ __global__ void __launch_bounds__(kGrThreads, 1)
       if (lane >= o) winc += y;
     }
     const uint32_t woff = __shfl_sync(0xffffffffu, winc - wc, warp);
-    if (tid == 31) a.segcnt[(int64_t)cur * a.ns_max + pc.j] = winc;   // the segment's total
+    if (tid == 31) {   // the segment's total and bound
+      a.segcnt[(int64_t)cur * a.ns_max + pc.j] = winc;
+      a.segbound[(int64_t)cur * a.ns_max + pc.j] = lo_key;
+    }
     if (m) {
       uint2* const ls = a.list + ((int64_t)cur * a.ns_max + pc.j) * kGrSeg;
       const uint32_t p0 = (uint32_t)(pc.A + 4 * tid - pc.g0);   // position of score q = 0
@@ -1785,16 +1794,16 @@ __global__ void __launch_bounds__(kGrThreads, 1)
   if (late && tid == 0) atomicOr(a.hdr + 2, 4u);
 
   // Every copy issued has been waited for: the ring's space becomes the two
-  // bitmaps and the staged output of phase 3.
+  // bitmaps and the staged output of phase 2.
   uint32_t* const sel = reinterpret_cast<uint32_t*>(gr_ring);
   uint32_t* const tie = sel + kGrWords;
   int32_t* const out_s = reinterpret_cast<int32_t*>(tie + kGrWords);
   for (int i = tid; i < 2 * kGrWords; i += kGrThreads) sel[i] = 0u;
   for (int i = tid; i < 3 * 256; i += kGrThreads) (&sm.h[0][0])[i] = 0u;
-  grid_barrier(a.hdr + 1, G, a.hdr + 2);
+  grid_barrier(a.hdr, G, a.hdr + 2);
   pdl_trigger();
 
-  // Phase 3: one CTA per row.
+  // Phase 2: one CTA per row.
   for (int r = blockIdx.x; r < R; r += (int)G) {
     grid_resolve(a, sm, sel, tie, out_s, r);
     __syncthreads();
@@ -1851,7 +1860,7 @@ cudaError_t launch_topk_grid(const float* scores, int64_t stride, int64_t rows,
   e = grid_ctas(dev, &G);
   if (e != cudaSuccess) return e;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  e = cudaMemsetAsync(ws, 0, gr_zero_bytes(rows), stream);
+  e = cudaMemsetAsync(ws, 0, kGrHeader, stream);
   if (e != cudaSuccess) return e;
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -1876,9 +1885,8 @@ cudaError_t launch_topk_grid(const float* scores, int64_t stride, int64_t rows,
   a.out = out;
   a.hdr = reinterpret_cast<uint32_t*>(ws);
   const int64_t nsm = gr_ns_max(stride);
-  a.hist = reinterpret_cast<uint32_t*>(ws + gr_hist_off());
-  a.segcnt = reinterpret_cast<uint32_t*>(ws + gr_segcnt_off(rows));
-  a.info = reinterpret_cast<uint2*>(ws + gr_info_off(rows, nsm));
+  a.segcnt = reinterpret_cast<uint32_t*>(ws + gr_segcnt_off());
+  a.segbound = reinterpret_cast<uint32_t*>(ws + gr_segbound_off(rows, nsm));
   a.list = reinterpret_cast<uint2*>(ws + gr_list_off(rows, nsm));
   a.ns_max = (int32_t)nsm;
   cudaLaunchConfig_t cfg = {};

@@ -111,17 +111,17 @@ def test_workspace_sizes(L):
 
 
 def test_topk_workspace_sizes(L):
-    # The grid top-k's workspace: a 256-byte header and a 4096-bin histogram
-    # per row (zeroed before each launch), an entry count per 8192-score
-    # segment, the per-row threshold, then one 8192-entry (key, position)
-    # slot per segment; a row has at most ceil((stride + 255) / 8192)
-    # segments. Shapes taken by the other kernels need none.
+    # The grid top-k's workspace: a 256-byte header (zeroed before each
+    # launch), an entry count and a key bound per 8192-score segment, then
+    # one 8192-entry (key, position) slot per segment; a row has at most
+    # ceil((stride + 255) / 8192) segments. Shapes taken by the other kernels
+    # need none.
     def al(b):
         return (b + 255) // 256 * 256
 
     def want(R, stride):
         ns = (stride + 255 + 8191) // 8192
-        return 256 + R * 4096 * 4 + al(R * ns * 4) + al(R * 8) + R * ns * 8192 * 8
+        return 256 + 2 * al(R * ns * 4) + R * ns * 8192 * 8
     for R, stride in [(128, 131072), (8, 100000), (1, 16384), (15, 32768), (255, 65536),
                       (16, 70000), (1, 8192)]:
         assert L.ds_topk_workspace_size(R, stride, 2048) == want(R, stride), (R, stride)
