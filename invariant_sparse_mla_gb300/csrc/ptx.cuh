@@ -94,19 +94,6 @@ __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* ma
       : "memory");
 }
 
-// One box of a 1D tensor map (elements x..) into shared memory at `dst`;
-// completion adds the box's bytes to `bar`'s transfer count. x times the
-// element size must be a multiple of 16 bytes; elements past the map's extent
-// arrive as zeros.
-__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* map, int x,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.1d.shared::cta.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2}], [%3];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // ---------------------------------------------------------------- cp.async
 // 16-byte global->shared copy through L2 only; src_bytes = 0 zero-fills.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
