@@ -1486,28 +1486,43 @@ __device__ __forceinline__ void grid_resolve(const GridArgs& a, GridSmem& sm, ui
   const uint2* __restrict__ lr = a.list + (int64_t)r * a.ns_max * kGrSeg;
   const float* __restrict__ srow = a.scores + sm.g0[r];
   bool whole = false;   // entries from the score row itself
-  auto entry = [&](uint32_t i) -> uint2 {
-    if (whole) return make_uint2(score_key(srow[i]), i);
-    int lo = 0, hi = ns;   // segpre[lo] <= i < segpre[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sm.segpre[mid] <= i) lo = mid;
-      else hi = mid;
-    }
-    uint2 v = __ldcg(lr + (int64_t)lo * kGrSeg + (i - sm.segpre[lo]));
-    if (v.y >= (uint32_t)L) v.y = kGrNoPos;
-    return v;
-  };
   uint2 e[kGrTileQ];
   // Slot q of tile t holds entry t * 8192 + q * 1024 + tid; entries below
-  // the bound M are not candidates.
+  // the bound M are not candidates. All of a thread's addresses are worked
+  // out before any load, so that its loads are in flight together.
   auto load_tile = [&](uint32_t t) {
+    uint32_t off[kGrTileQ];
 #pragma unroll
     for (int q = 0; q < kGrTileQ; ++q) {
       const uint32_t i = t * kGrTile + (uint32_t)(q * kGrThreads + tid);
-      e[q] = i < n ? entry(i) : make_uint2(0u, kGrNoPos);
-      if (e[q].x < mkey) e[q].y = kGrNoPos;
+      off[q] = i;
+      if (!whole && i < n) {
+        int lo = 0, hi = ns;   // segpre[lo] <= i < segpre[hi]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (sm.segpre[mid] <= i) lo = mid;
+          else hi = mid;
+        }
+        off[q] = (uint32_t)lo * kGrSeg + (i - sm.segpre[lo]);
+      }
     }
+    if (whole) {
+#pragma unroll
+      for (int q = 0; q < kGrTileQ; ++q) {
+        const uint32_t i = t * kGrTile + (uint32_t)(q * kGrThreads + tid);
+        e[q] = i < n ? make_uint2(score_key(srow[i]), i) : make_uint2(0u, kGrNoPos);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kGrTileQ; ++q) {
+        const uint32_t i = t * kGrTile + (uint32_t)(q * kGrThreads + tid);
+        e[q] = i < n ? __ldcg(lr + off[q]) : make_uint2(0u, kGrNoPos);
+        if (e[q].y >= (uint32_t)L) e[q].y = kGrNoPos;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kGrTileQ; ++q)
+      if (e[q].x < mkey) e[q].y = kGrNoPos;
   };
   uint32_t ntiles = (n + kGrTile - 1) / kGrTile;
   uint32_t mine = 0u;
