@@ -343,3 +343,32 @@ def test_grid_kernel_batch_of_one_row_in_many(ds):
         b[slot] = 60001
         got = _grid_run(ds, s, a, b, k)
         assert np.array_equal(got[slot], ref), B
+
+
+def test_grid_kernel_bound_edge_cases(ds):
+    # Rows built against the bound each CTA takes from the first segment of
+    # its part of a row: a first segment of NaN (the bound drops to the
+    # bottom: everything after it is listed), the largest scores at the end
+    # of the row (early bounds low, lists long but complete), +inf first and
+    # falling after (the bound lies above most of the top k, so the row is
+    # taken whole), every score tied, and a row one longer than k.
+    rng = np.random.default_rng(33)
+    R, stride, k = 10, 100000, 2048
+    s = rng.standard_normal((R, stride)).astype(np.float32)
+    a = np.zeros(R, np.int64)
+    b = np.full(R, stride, np.int64)
+    s[0, :9000] = np.nan
+    s[1] = np.sort(s[1])                       # ascending: the top k is the row's end
+    s[2, :3000] = np.inf
+    s[2, 3000:] = -np.sort(-s[2, 3000:])       # descending after the infinities
+    s[3] = 7.0                                 # all tied
+    b[4] = k + 1
+    s[5, ::2] = np.nan                         # half NaN
+    s[6] = np.where(rng.random(stride) < 0.5, 0.0, -0.0).astype(np.float32)
+    s[6, 50000:50010] = 1.0
+    s[7, :8192] = -np.inf
+    a[8], b[8] = 1, stride - 1                 # odd start and end
+    s[9, -5000:] = 100.0 + rng.standard_normal(5000).astype(np.float32)
+    got = _grid_run(ds, s, a, b, k)
+    want = oracle.topk_per_row(s, a, b, k)
+    assert np.array_equal(got, want), np.nonzero((got != want).any(1))[0][:10].tolist()
