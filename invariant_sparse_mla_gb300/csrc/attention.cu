@@ -878,16 +878,13 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
 // Merges the splits of one (row, head) in split order (merge_weights,
 // merge_value), reading the partial results from the workspace. Every split's
 // m, l and O slice is loaded in one round before any arithmetic.
-__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ part_o,
-                                                      const float* __restrict__ part_m,
+__device__ __forceinline__ void combine_one(int64_t rh, const uint16_t* __restrict__ part_o,
+                                            const float* __restrict__ part_m,
                                                       const float* __restrict__ part_l,
                                                       int64_t R, int H, int S,
                                                       const float* __restrict__ sink,
                                                       __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ lse) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t rh = blockIdx.x;  // row * H + h
   const int t = threadIdx.x;
   const int64_t RH = R * H;
   float ms[kMaxSplits], ls[kMaxSplits];
@@ -934,6 +931,31 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
   r.y = pack_bf16x2(v[2], v[3]);
   *reinterpret_cast<uint2*>(o) = r;
   if (t == 0) lse[rh] = mw.lse;
+}
+
+// (row, head) pairs from which the combine takes four pairs per CTA: about
+// four waves of one-pair CTAs (16 resident per SM on 152 SMs).
+constexpr int64_t kCombineWideFrom = 8192;
+
+// One CTA of 128 threads merges U consecutive (row, head) pairs, one after
+// the other. U changes only how the pairs are spread over CTAs: a large batch
+// (many waves of CTAs at U = 1) takes U = 4, so that fewer CTAs are launched;
+// each pair's arithmetic is the same either way.
+template <int U>
+__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ part_o,
+                                                      const float* __restrict__ part_m,
+                                                      const float* __restrict__ part_l,
+                                                      int64_t R, int H, int S,
+                                                      const float* __restrict__ sink,
+                                                      __nv_bfloat16* __restrict__ out,
+                                                      float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t rh = (int64_t)blockIdx.x * U + u;   // row * H + h
+    if (rh < R * H) combine_one(rh, part_o, part_m, part_l, R, H, S, sink, out, lse);
+  }
 }
 
 template <int HG, bool FP8>
@@ -1028,7 +1050,13 @@ cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream) {
   else
     e = fp8 ? launch_split<16, true>(kp, blocks, stream) : launch_split<16, false>(kp, blocks, stream);
   if (e != cudaSuccess) return e;
-  return launch_pdl(combine_kernel, dim3((unsigned)(a.R * a.H)), dim3(128), 0, stream, 1u,
+  const int64_t RH = a.R * a.H;
+  if (RH >= kCombineWideFrom)
+    return launch_pdl(combine_kernel<4>, dim3((unsigned)((RH + 3) / 4)), dim3(128), 0, stream, 1u,
+                      (const uint16_t*)ws.part_o, (const float*)ws.part_m, (const float*)ws.part_l,
+                      a.R, a.H, kp.num_splits, a.sink, reinterpret_cast<__nv_bfloat16*>(a.out),
+                      a.lse);
+  return launch_pdl(combine_kernel<1>, dim3((unsigned)RH), dim3(128), 0, stream, 1u,
                     (const uint16_t*)ws.part_o, (const float*)ws.part_m, (const float*)ws.part_l, a.R,
                     a.H, kp.num_splits, a.sink, reinterpret_cast<__nv_bfloat16*>(a.out), a.lse);
 }
