@@ -372,3 +372,46 @@ def test_grid_kernel_bound_edge_cases(ds):
     got = _grid_run(ds, s, a, b, k)
     want = oracle.topk_per_row(s, a, b, k)
     assert np.array_equal(got, want), np.nonzero((got != want).any(1))[0][:10].tolist()
+
+
+def test_grid_kernel_in_a_cuda_graph(ds):
+    # The cooperative launch and the workspace header's zero fill capture into
+    # a CUDA graph; replays on new scores in the same buffers give the
+    # oracle's indices each time.
+    rng = np.random.default_rng(41)
+    R, stride, k = 24, 90000, 2048
+    s0, a, b = _mixed_rows(rng, R, stride, k)
+    scores = torch.as_tensor(s0).to(DEV)
+    starts = torch.as_tensor(a, dtype=torch.int32).to(DEV)
+    ends = torch.as_tensor(b, dtype=torch.int32).to(DEV)
+    ws = torch.empty(ds.topk_workspace_size(R, stride, k), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((R, k), dtype=torch.int32, device=DEV)
+    side = torch.cuda.Stream(DEV)
+    with torch.cuda.stream(side):
+        ds.topk_per_row(scores, starts, ends, k, idx_out=idx, workspace=ws)   # warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        ds.topk_per_row(scores, starts, ends, k, idx_out=idx, workspace=ws)
+    for it in range(3):
+        s = rng.standard_normal((R, stride)).astype(np.float32) if it else s0
+        scores.copy_(torch.as_tensor(s))
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(ws[8:12].view(torch.int32).item()) == 0
+        assert np.array_equal(idx.cpu().numpy(), oracle.topk_per_row(s, a, b, k)), it
+
+
+def test_grid_kernel_k1_and_short_workspace(ds):
+    rng = np.random.default_rng(42)
+    R, stride = 6, 70000
+    s, a, b = _mixed_rows(rng, R, stride, 1)
+    assert np.array_equal(_grid_run(ds, s, a, b, 1), oracle.topk_per_row(s, a, b, 1))
+    # One byte short of the grid kernel's workspace: a workspace-free kernel
+    # runs instead, with the same indices.
+    k = 700
+    s, a, b = _mixed_rows(rng, R, stride, k)
+    need = ds.topk_workspace_size(R, stride, k)
+    short = torch.empty(need - 1, dtype=torch.uint8, device=DEV)
+    got = run(ds, s, a, b, k, workspace=short)
+    assert np.array_equal(got, oracle.topk_per_row(s, a, b, k))
