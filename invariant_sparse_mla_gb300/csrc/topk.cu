@@ -1225,7 +1225,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) topk_stream_
 //      per segment issued by one thread and completing on the stage's
 //      mbarrier. On the first segment of each row it touches (n in-row
 //      scores) it takes a bound B: the 12-bit prefix bin holding the
-//      segment's (2 k n / L + 32)-th largest key (every key when n is
+//      segment's (3 k n / 2L + 32)-th largest key (every key when n is
 //      smaller), a generous estimate of where the row's k-th largest key
 //      lies. It then lists every score of its part of the row whose key is
 //      at least B << 20, with its position: segment j of a row has its own
@@ -1738,7 +1738,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
     }
     if (first) {
       // The bound from this segment's n in-row scores: the bin of its
-      // (2 k n / L + 32)-th largest key.
+      // (3 k n / 2L + 32)-th largest key.
 #pragma unroll
       for (int q = 0; q < kGrPer; ++q)
         if ((valid >> q) & 1u) atomicAdd(&sm.hist[score_key(x[q]) >> 20], 1u);
@@ -1746,7 +1746,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
       const int32_t lo_e = pc.A > pc.g0 ? pc.A : pc.g0;
       const int32_t hi_e = pc.A + kGrSeg < pc.gend ? pc.A + kGrSeg : pc.gend;
       const uint32_t nseg = (uint32_t)(hi_e - lo_e);
-      uint64_t t1 = 2ull * k * nseg / (uint64_t)(pc.gend - pc.g0) + 32u;
+      uint64_t t1 = 3ull * k * nseg / (2ull * (uint64_t)(pc.gend - pc.g0)) + 32u;
       if (t1 > nseg) t1 = nseg;
       gr_pick4096(sm, (uint32_t)t1);
       const uint32_t B = sm.pick[0];
