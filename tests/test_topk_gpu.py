@@ -415,3 +415,41 @@ def test_grid_kernel_k1_and_short_workspace(ds):
     short = torch.empty(need - 1, dtype=torch.uint8, device=DEV)
     got = run(ds, s, a, b, k, workspace=short)
     assert np.array_equal(got, oracle.topk_per_row(s, a, b, k))
+
+
+def test_grid_kernel_random_shapes(ds):
+    # Seeded random shapes, bounds and score distributions (normal, few
+    # distinct integers, special values, eighths with NaN holes, sorted rows,
+    # a narrow band of shared high bits), each against the oracle.
+    rng = np.random.default_rng(2027)
+    specials = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan], np.float32)
+    done = 0
+    while done < 24:
+        R = int(rng.choice([1, 3, 8, 15, 40, 100]))
+        stride = int(rng.integers(max(8192 // R + 1, 64), 131073))
+        if R * stride > (1 << 20):
+            stride = (1 << 20) // R
+        k = int(rng.choice([1, 7, 100, 700, 2048, 2049, 8192]))
+        if ds.topk_workspace_size(R, stride, k) == 0:
+            continue
+        kind = done % 6
+        if kind == 0:
+            s = rng.standard_normal((R, stride)).astype(np.float32)
+        elif kind == 1:
+            s = rng.integers(0, int(rng.integers(1, 50)), (R, stride)).astype(np.float32)
+        elif kind == 2:
+            s = rng.choice(specials, (R, stride))
+        elif kind == 3:
+            s = (np.round(rng.standard_normal((R, stride)) * 8) / 8).astype(np.float32)
+            s[rng.random((R, stride)) < 0.1] = np.nan
+        elif kind == 4:
+            s = np.sort(rng.standard_normal((R, stride)).astype(np.float32), axis=1)
+            if rng.random() < 0.5:
+                s = s[:, ::-1].copy()
+        else:
+            s = (1.0 + rng.random((R, stride)) * 2.0 ** -int(rng.integers(5, 20))).astype(np.float32)
+        a = rng.integers(-3, stride // 3, R)
+        b = a + rng.integers(-5, stride + 10, R)
+        got = _grid_run(ds, s, a, b, k)
+        assert np.array_equal(got, oracle.topk_per_row(s, a, b, k)), (R, stride, k, kind)
+        done += 1
