@@ -22,9 +22,14 @@ LSE_ATOL = 1e-2
 # split's partial output before the merge (another 2^-9), P is rounded to
 # bf16 before PV (<= 2^-9 relative per entry, averaging out over the
 # entries), and FP8 rows are dequantised to bf16 (another 2^-9 relative on
-# every K and V element). That predicts about 0.015-0.02 RMS; measured up to
-# 0.026 (bf16) and 0.028 (FP8) over the parity cases, under the bounds.
-RMS_TOL = {"bf16": 2 ** -5, "fp8": 2 ** -4}
+# every K and V element). That predicts about 0.015-0.02 RMS for typical
+# heads; a head whose output has a few large dims (max/RMS well above 4)
+# reaches further. Measured up to 0.026 (bf16) and 0.028 (FP8) over the
+# parity cases, and up to 0.035 (bf16) and 0.039 (FP8) over 1426 random
+# decode shapes (heads 16-128, k 64-2048, both pools, invalid entries), so
+# the bf16 bound is 3 * 2^-6: above that tail, and still far below the 8 %
+# scaling error of test_harness_cpu.
+RMS_TOL = {"bf16": 3 * 2 ** -6, "fp8": 2 ** -4}
 
 
 def ensure_built():
