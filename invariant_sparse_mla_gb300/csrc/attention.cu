@@ -875,87 +875,66 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1) sparse_mla_split_kern
   if (warp == RL::kQkA) tmem_dealloc(tmem, LY::kTmemCols);
 }
 
-// Merges the splits of one (row, head) in split order (merge_weights,
-// merge_value), reading the partial results from the workspace. Every split's
-// m, l and O slice is loaded in one round before any arithmetic.
-__device__ __forceinline__ void combine_one(int64_t rh, const uint16_t* __restrict__ part_o,
-                                            const float* __restrict__ part_m,
-                                                      const float* __restrict__ part_l,
-                                                      int64_t R, int H, int S,
-                                                      const float* __restrict__ sink,
-                                                      __nv_bfloat16* __restrict__ out,
-                                                      float* __restrict__ lse) {
-  const int t = threadIdx.x;
+// The combine: one warp merges the splits of one (row, head) pair in split
+// order (merge_weights once per pair, merge_value per output element). Lane l
+// takes output columns [16 l, 16 l + 16): two 16-byte loads of bf16 partials
+// per split, all of them (128 bytes per lane) issued before any arithmetic.
+// W warps (pairs) per CTA; which warp takes a pair never changes its
+// arithmetic.
+template <int W>
+__global__ void __launch_bounds__(32 * W) combine_warp_kernel(const uint16_t* __restrict__ part_o,
+                                                              const float* __restrict__ part_m,
+                                                              const float* __restrict__ part_l,
+                                                              int64_t R, int H, int S,
+                                                              const float* __restrict__ sink,
+                                                              __nv_bfloat16* __restrict__ out,
+                                                              float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
   const int64_t RH = R * H;
+  const int64_t rh = (int64_t)blockIdx.x * W + (threadIdx.x >> 5);   // row * H + h
+  if (rh >= RH) return;
   float ms[kMaxSplits], ls[kMaxSplits];
-  float4 os[kMaxSplits];
+  uint4 raw[kMaxSplits][2];
 #pragma unroll
   for (int s = 0; s < kMaxSplits; ++s) {
     ms[s] = -INFINITY;
     ls[s] = 0.0f;
-    os[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+    raw[s][0] = raw[s][1] = make_uint4(0u, 0u, 0u, 0u);
     if (s < S) {
       ms[s] = part_m[s * RH + rh];
       ls[s] = part_l[s * RH + rh];
-      const uint2 w = *reinterpret_cast<const uint2*>(part_o + (s * RH + rh) * kDv + 4 * t);
-      os[s] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                          __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+      const uint4* p = reinterpret_cast<const uint4*>(part_o + (s * RH + rh) * kDv + 16 * lane);
+      raw[s][0] = p[0];
+      raw[s][1] = p[1];
     }
   }
   const float sl = sink != nullptr ? sink[rh % H] * 1.4426950408889634f : -INFINITY;
   const MergeWeights mw = merge_weights(ms, ls, sl);
-  __nv_bfloat16* o = out + rh * kDv + 4 * t;
-  if (mw.state == 2) {   // a split that timed out left NaN partials
-    *reinterpret_cast<uint2*>(o) = make_uint2(0x7fc07fc0u, 0x7fc07fc0u);
-    if (t == 0) lse[rh] = __int_as_float(0x7fc00000);
+  uint4* o = reinterpret_cast<uint4*>(out + rh * kDv + 16 * lane);
+  if (mw.state != 0) {   // 2: a split gave up (NaN); 1: no entry (0, lse -inf)
+    const uint32_t f = mw.state == 2 ? 0x7fc07fc0u : 0u;
+    o[0] = o[1] = make_uint4(f, f, f, f);
+    if (lane == 0) lse[rh] = mw.state == 2 ? __int_as_float(0x7fc00000) : -INFINITY;
     return;
   }
-  if (mw.state == 1) {
-    *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
-    if (t == 0) lse[rh] = -INFINITY;
-    return;
-  }
-  float v[4];
-  {
-    const float o0[kMaxSplits] = {os[0].x, os[1].x, os[2].x, os[3].x};
-    const float o1[kMaxSplits] = {os[0].y, os[1].y, os[2].y, os[3].y};
-    const float o2[kMaxSplits] = {os[0].z, os[1].z, os[2].z, os[3].z};
-    const float o3[kMaxSplits] = {os[0].w, os[1].w, os[2].w, os[3].w};
-    v[0] = merge_value(mw, o0);
-    v[1] = merge_value(mw, o1);
-    v[2] = merge_value(mw, o2);
-    v[3] = merge_value(mw, o3);
-  }
-  uint2 r;
-  r.x = pack_bf16x2(v[0], v[1]);
-  r.y = pack_bf16x2(v[2], v[3]);
-  *reinterpret_cast<uint2*>(o) = r;
-  if (t == 0) lse[rh] = mw.lse;
-}
-
-// (row, head) pairs from which the combine takes four pairs per CTA: about
-// four waves of one-pair CTAs (16 resident per SM on 152 SMs).
-constexpr int64_t kCombineWideFrom = 8192;
-
-// One CTA of 128 threads merges U consecutive (row, head) pairs, one after
-// the other. U changes only how the pairs are spread over CTAs: a large batch
-// (many waves of CTAs at U = 1) takes U = 4, so that fewer CTAs are launched;
-// each pair's arithmetic is the same either way.
-template <int U>
-__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ part_o,
-                                                      const float* __restrict__ part_m,
-                                                      const float* __restrict__ part_l,
-                                                      int64_t R, int H, int S,
-                                                      const float* __restrict__ sink,
-                                                      __nv_bfloat16* __restrict__ out,
-                                                      float* __restrict__ lse) {
-  pdl_wait();
-  pdl_trigger();
+  uint32_t packed[8];
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int64_t rh = (int64_t)blockIdx.x * U + u;   // row * H + h
-    if (rh < R * H) combine_one(rh, part_o, part_m, part_l, R, H, S, sink, out, lse);
+  for (int j = 0; j < 8; ++j) {   // word j holds elements 2j (low half) and 2j + 1
+    float lo[kMaxSplits], hi[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+      const uint4& q = raw[s][j >> 2];
+      const uint32_t w = (j & 3) == 0 ? q.x : (j & 3) == 1 ? q.y : (j & 3) == 2 ? q.z : q.w;
+      lo[s] = __uint_as_float(w << 16);
+      hi[s] = __uint_as_float(w & 0xffff0000u);
+    }
+    packed[j] = pack_bf16x2(merge_value(mw, lo), merge_value(mw, hi));
   }
+  o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  if (lane == 0) lse[rh] = mw.lse;
 }
 
 template <int HG, bool FP8>
@@ -1051,12 +1030,7 @@ cudaError_t launch_sparse_mla(const AttnArgs& a, cudaStream_t stream) {
     e = fp8 ? launch_split<16, true>(kp, blocks, stream) : launch_split<16, false>(kp, blocks, stream);
   if (e != cudaSuccess) return e;
   const int64_t RH = a.R * a.H;
-  if (RH >= kCombineWideFrom)
-    return launch_pdl(combine_kernel<4>, dim3((unsigned)((RH + 3) / 4)), dim3(128), 0, stream, 1u,
-                      (const uint16_t*)ws.part_o, (const float*)ws.part_m, (const float*)ws.part_l,
-                      a.R, a.H, kp.num_splits, a.sink, reinterpret_cast<__nv_bfloat16*>(a.out),
-                      a.lse);
-  return launch_pdl(combine_kernel<1>, dim3((unsigned)RH), dim3(128), 0, stream, 1u,
+  return launch_pdl(combine_warp_kernel<8>, dim3((unsigned)((RH + 7) / 8)), dim3(256), 0, stream, 1u,
                     (const uint16_t*)ws.part_o, (const float*)ws.part_m, (const float*)ws.part_l, a.R,
                     a.H, kp.num_splits, a.sink, reinterpret_cast<__nv_bfloat16*>(a.out), a.lse);
 }
