@@ -78,16 +78,18 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) kv_write_fp8_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + warp;
   if (row >= n) return;
+  // The row's loads go out together with its slot's (a padding row's latent
+  // is read and dropped), so a row costs one memory round trip, not two.
   const int64_t slot = slots[row];
+  const uint4* src = latent + row * kRowChunks;
+  const uint4 c0 = src[lane], c1 = src[lane + 32];
+  uint4 rope = make_uint4(0u, 0u, 0u, 0u);
+  if (lane < 8) rope = src[kLatentChunks + lane];
   if (slot < 0) return;   // padding row
   if (slot >= num_slots) {
     if (lane == 0 && err != nullptr) atomicOr(err, kErrPage);
     return;
   }
-  const uint4* src = latent + row * kRowChunks;
-  const uint4 c0 = src[lane], c1 = src[lane + 32];
-  uint4 rope = make_uint4(0u, 0u, 0u, 0u);
-  if (lane < 8) rope = src[kLatentChunks + lane];
   float x0[8], x1[8];
   bf16x8_to_float(c0, x0);
   bf16x8_to_float(c1, x1);
@@ -114,14 +116,19 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) kv_write_bf16_kernel(
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + warp;
   if (row >= n) return;
   const int64_t slot = slots[row];
+  const uint4* src = latent + row * kRowChunks;
+  const uint4 c0 = src[lane], c1 = src[lane + 32];   // chunks lane, lane + 32
+  uint4 c2 = make_uint4(0u, 0u, 0u, 0u);             // chunk lane + 64 (lanes 0-7)
+  if (lane < kRowChunks - 64) c2 = src[lane + 64];
   if (slot < 0) return;
   if (slot >= num_slots) {
     if (lane == 0 && err != nullptr) atomicOr(err, kErrPage);
     return;
   }
-  const uint4* src = latent + row * kRowChunks;
   uint4* dst = pool + slot * kRowChunks;
-  for (int c = lane; c < kRowChunks; c += 32) dst[c] = src[c];
+  dst[lane] = c0;
+  dst[lane + 32] = c1;
+  if (lane < kRowChunks - 64) dst[lane + 64] = c2;
 }
 
 }  // namespace
