@@ -3,8 +3,9 @@
 New latent rows go to slots page * 64 + offset of a paged pool; FP8 pools get
 the quantised layout (E4M3 codes, four contiguous fp32 group scales, bf16
 rope). Covers random rows, all-zero and single-value groups, values that
-saturate or fall to subnormal codes, signed zeros, padding slots (-1, never
-written), slots past the pool (flagged, not written), untouched slots, and a
+saturate or fall to subnormal codes, signed zeros, quotients on and next to
+E4M3 rounding midpoints under scales with inexact reciprocals, padding slots
+(-1, never written), slots past the pool (flagged, not written), untouched slots, and a
 read-back through the FP8 attention path.
 """
 
@@ -63,6 +64,46 @@ def test_cache_write_exact(ds, kv_dtype):
     bad = np.nonzero((got != want).reshape(pages * 64, -1).any(1))[0]
     assert bad.size == 0, f"slots differ: {bad[:10].tolist()}"
     assert flagged and int(err.item()) == ds.DEVERR_PAGE
+
+
+def _boundary_rows(n, seed):
+    """bf16 latent rows whose groups have scales odd * 2**k (amax = 448 * scale,
+    exactly representable) and whose other values are bf16(scale * v) and its
+    bf16 neighbours, v an E4M3 value or a midpoint between two: quotients on or
+    within a few float32 units of E4M3 rounding boundaries, where a quotient
+    taken as x * (1 / scale) can round to another code than x / scale."""
+    rng = np.random.default_rng(seed)
+    vals = oracle.e4m3_to_float64(np.arange(0x7F, dtype=np.uint8))
+    targets = np.concatenate([vals, (vals[:-1] + vals[1:]) / 2])
+    odds = [3, 5, 7, 9, 11, 13, 15, 17, 19, 21, 23, 25, 27, 29, 31, 33, 35]
+    bits = np.zeros((n, 576), np.uint16)
+    for r in range(n):
+        for g in range(4):
+            scale = float(rng.choice(odds)) * 2.0 ** int(rng.integers(-24, 25))
+            amax = np.float32(448.0 * scale)
+            v = rng.choice(targets, 127) * scale * rng.choice([-1.0, 1.0], 127)
+            b = (np.asarray(v, np.float32).view(np.uint32) + 0x8000) >> 16   # to bf16 (half up)
+            b = (b.astype(np.int64) + rng.integers(-1, 2, 127)) & 0xFFFF       # a bf16 step either way
+            x = (b.astype(np.uint32) << 16).view(np.float32)
+            b = np.where(np.abs(x) <= amax, b, 0)                              # keep |x| <= amax
+            row = np.concatenate([[amax.view(np.uint32) >> 16], b]).astype(np.uint16)
+            bits[r, 128 * g:128 * (g + 1)] = rng.permutation(row)
+        bits[r, 512:] = rng.integers(0, 0x7F00, 64)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def test_cache_write_fp8_rounding_boundaries(ds):
+    # Quotients at and next to E4M3 rounding midpoints, under scales whose
+    # reciprocals are inexact: every code still matches the float32 division.
+    n = 512
+    latent = _boundary_rows(n, 21).to(DEV)
+    pool = torch.zeros((n // 64, 64, 656), dtype=torch.uint8, device=DEV)
+    ds.kv_cache_write(latent, torch.arange(n, device=DEV), pool, "fp8")
+    torch.cuda.synchronize()
+    want = oracle.quantize_latent_rows(_bits(latent.cpu()))
+    got = kv_np(pool, "fp8").reshape(n, 656)
+    bad = np.nonzero((got != want).any(1))[0]
+    assert bad.size == 0, f"rows differ: {bad[:10].tolist()}"
 
 
 def test_written_fp8_rows_read_back_through_attention(ds):
