@@ -30,7 +30,8 @@ def e4m3_to_float64(codes):
 def bf16_bits_to_float64(bits):
     """Decode uint16 bfloat16 bit patterns to float64 (exact)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return b.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):   # signalling-NaN patterns convert to NaN, as they should
+        return b.view(np.float32).astype(np.float64)
 
 
 # ---------------------------------------------------------------- encoding
